@@ -1,0 +1,276 @@
+"""ctypes binding of libgrbeam (include/grbeam.h): argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels.  PyTorch
+supplies device memory and the current CUDA stream.  If the shared library is
+missing the import of this module still works, but the first call raises
+``RuntimeError``: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libgrbeam.so")
+
+GR_OK = 0
+GR_ERR_INVALID_ARG = -1
+GR_ERR_UNSUPPORTED = -2
+GR_ERR_CAPACITY = -3
+GR_ERR_STATE = -4
+GR_ERR_CUDA = -5
+GR_ERR_TIMEOUT = -6
+GR_ERR_DEVICE = -7
+
+KERNEL_CTX_ATTN = 0
+KERNEL_BEAM_ATTN = 1
+KERNEL_LOGSOFTMAX = 2
+KERNEL_TOPK = 3
+KERNEL_ADVANCE = 4
+KERNEL_RESULTS = 5
+KERNEL_INIT = 6
+KERNEL_KINDS = 7
+KERNEL_NAMES = ["ctx_attn", "beam_attn", "logsoftmax_gather", "topk_select", "advance", "results", "init"]
+
+# exported symbols of include/grbeam.h
+SYMBOLS = [
+    "gr_trie_device_bytes", "gr_trie_create", "gr_trie_destroy",
+    "gr_beam_workspace_bytes", "gr_beam_kv_bytes", "gr_beam_create", "gr_beam_destroy",
+    "gr_beam_rows", "gr_beam_step", "gr_beam_kv_slot", "gr_decode_attn", "gr_constrained_topk",
+    "gr_beam_advance", "gr_beam_rewind", "gr_beam_results", "gr_beam_path", "gr_beam_status",
+    "gr_beam_set_timing", "gr_beam_kernel_stats", "gr_beam_set_wait_limit",
+    "gr_status_str", "gr_last_error",
+]
+
+
+class GrConfig(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("vocab", ctypes.c_int), ("code_base", ctypes.c_int),
+                ("n_levels", ctypes.c_int), ("codes_per_level", ctypes.c_int), ("pool_tokens", ctypes.c_int64)]
+
+
+class GrRequest(ctypes.Structure):
+    _fields_ = [("ctx_offset", ctypes.c_int64), ("ctx_len", ctypes.c_int), ("beam_width", ctypes.c_int),
+                ("trie", ctypes.c_void_p)]
+
+
+class GrBuffers(ctypes.Structure):
+    _fields_ = [("ctx_k", ctypes.c_void_p), ("ctx_v", ctypes.c_void_p), ("beam_k", ctypes.c_void_p),
+                ("beam_v", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class GrError(RuntimeError):
+    def __init__(self, status: int, name: str, message: str):
+        super().__init__(f"{name}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libgrbeam is not built ({LIB_PATH} missing): run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        c_int, c_i64, vp, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+        P = ctypes.POINTER
+        sig = {
+            "gr_trie_device_bytes": [vp, c_i64, c_int, c_int, P(sz)],
+            "gr_trie_create": [vp, vp, c_i64, c_int, c_int, vp, sz, vp, P(vp)],
+            "gr_trie_destroy": [vp],
+            "gr_beam_workspace_bytes": [P(GrConfig), P(GrRequest), c_int, P(sz)],
+            "gr_beam_kv_bytes": [P(GrConfig), P(GrRequest), c_int, P(sz)],
+            "gr_beam_create": [P(GrConfig), P(GrRequest), c_int, P(GrBuffers), vp, P(vp)],
+            "gr_beam_destroy": [vp],
+            "gr_beam_rows": [vp, P(c_int), vp],
+            "gr_beam_step": [vp, P(c_int)],
+            "gr_beam_kv_slot": [vp, c_int, P(vp), P(vp)],
+            "gr_decode_attn": [vp, c_int, vp, vp, vp],
+            "gr_constrained_topk": [vp, vp, c_i64, vp, vp, vp, vp],
+            "gr_beam_advance": [vp, vp],
+            "gr_beam_rewind": [vp, c_int],
+            "gr_beam_results": [vp, c_int, vp, vp, vp, P(c_int), vp],
+            "gr_beam_path": [vp, c_int, c_int, vp, vp, vp, vp, P(c_int), vp],
+            "gr_beam_status": [vp, c_int, vp],
+            "gr_beam_set_timing": [vp, c_int],
+            "gr_beam_kernel_stats": [vp, c_int, P(c_i64), P(ctypes.c_double), c_int],
+            "gr_beam_set_wait_limit": [vp, c_i64],
+            "gr_status_str": [c_int],
+            "gr_last_error": [],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = c_int
+        L.gr_status_str.restype = ctypes.c_char_p
+        L.gr_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def check(status: int) -> None:
+    if status != GR_OK:
+        L = lib()
+        raise GrError(status, L.gr_status_str(status).decode(), L.gr_last_error().decode())
+
+
+def _stream_ptr(stream=None) -> ctypes.c_void_p:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+class Trie:
+    """Item catalogue uploaded into a torch-owned device buffer."""
+
+    def __init__(self, codes: np.ndarray, item_ids: Optional[np.ndarray] = None, codes_per_level: int = 256,
+                 device="cuda"):
+        import torch
+        codes = np.ascontiguousarray(codes, dtype=np.int32)
+        n, L = codes.shape
+        self.n_levels, self.codes_per_level, self.n_items = L, codes_per_level, n
+        ids = None if item_ids is None else np.ascontiguousarray(item_ids, dtype=np.int64)
+        nbytes = ctypes.c_size_t()
+        check(lib().gr_trie_device_bytes(codes.ctypes.data, n, L, codes_per_level, ctypes.byref(nbytes)))
+        self.buffer = torch.empty(max(nbytes.value, 256), dtype=torch.uint8, device=device)
+        h = ctypes.c_void_p()
+        check(lib().gr_trie_create(codes.ctypes.data, None if ids is None else ids.ctypes.data, n, L,
+                                   codes_per_level, self.buffer.data_ptr(), self.buffer.numel(), _stream_ptr(),
+                                   ctypes.byref(h)))
+        self.handle = h
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.gr_trie_destroy(self.handle)
+            self.handle = None
+
+
+class Beam:
+    """One batch of requests being decoded (gr_beam handle + its device buffers)."""
+
+    def __init__(self, n_layers: int, n_q_heads: int, n_kv_heads: int, head_dim: int, vocab: int,
+                 code_base: int, n_levels: int, codes_per_level: int, ctx_k, ctx_v,
+                 requests: Sequence[Tuple[int, int, int, Trie]], device="cuda"):
+        """ctx_k / ctx_v: bf16 tensors [n_layers, n_kv_heads, pool_tokens, head_dim];
+        requests: (ctx_offset, ctx_len, beam_width, trie) per request."""
+        import torch
+        assert ctx_k.dtype == torch.bfloat16 and ctx_v.dtype == torch.bfloat16
+        assert ctx_k.is_contiguous() and ctx_v.is_contiguous()
+        self.cfg = GrConfig(n_layers, n_q_heads, n_kv_heads, head_dim, vocab, code_base, n_levels,
+                            codes_per_level, ctx_k.shape[2])
+        n = len(requests)
+        self.reqs = (GrRequest * n)(*[GrRequest(o, l, w, t.handle) for (o, l, w, t) in requests])
+        self.tries = [t for (_, _, _, t) in requests]
+        self.ctx_k, self.ctx_v = ctx_k, ctx_v
+        self.n_requests = n
+        self.widths = [w for (_, _, w, _) in requests]
+        self.rows = sum(self.widths)
+        ws = ctypes.c_size_t()
+        check(lib().gr_beam_workspace_bytes(ctypes.byref(self.cfg), self.reqs, n, ctypes.byref(ws)))
+        kvb = ctypes.c_size_t()
+        check(lib().gr_beam_kv_bytes(ctypes.byref(self.cfg), self.reqs, n, ctypes.byref(kvb)))
+        self.workspace = torch.empty(ws.value, dtype=torch.uint8, device=device)
+        shape = (n_layers, max(n_levels - 1, 1), self.rows, n_kv_heads, head_dim)
+        self.beam_k = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.beam_v = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        assert kvb.value <= self.beam_k.numel() * 2
+        bufs = GrBuffers(ctx_k.data_ptr(), ctx_v.data_ptr(), self.beam_k.data_ptr(), self.beam_v.data_ptr(),
+                         self.workspace.data_ptr(), self.workspace.numel())
+        h = ctypes.c_void_p()
+        check(lib().gr_beam_create(ctypes.byref(self.cfg), self.reqs, n, ctypes.byref(bufs), _stream_ptr(),
+                                   ctypes.byref(h)))
+        self.handle = h
+        offs = (ctypes.c_int * (n + 1))()
+        rows = ctypes.c_int()
+        check(lib().gr_beam_rows(self.handle, ctypes.byref(rows), offs))
+        self.row_offsets = list(offs)
+        assert rows.value == self.rows
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.gr_beam_destroy(self.handle)
+            self.handle = None
+
+    # -- state -------------------------------------------------------------
+    @property
+    def step(self) -> int:
+        s = ctypes.c_int()
+        check(lib().gr_beam_step(self.handle, ctypes.byref(s)))
+        return s.value
+
+    def kv_slot(self, layer: int):
+        """(k_new, v_new) views [rows, n_kv_heads, head_dim] of the open BeamKV level."""
+        k, v = ctypes.c_void_p(), ctypes.c_void_p()
+        check(lib().gr_beam_kv_slot(self.handle, layer, ctypes.byref(k), ctypes.byref(v)))
+        t = self.step
+        kk, vv = self.beam_k[layer, t - 1], self.beam_v[layer, t - 1]
+        assert kk.data_ptr() == k.value and vv.data_ptr() == v.value
+        return kk, vv
+
+    # -- hot path ------------------------------------------------------------
+    def decode_attn(self, layer: int, q, out, stream=None) -> None:
+        check(lib().gr_decode_attn(self.handle, layer, q.data_ptr(), out.data_ptr(), _stream_ptr(stream)))
+
+    def constrained_topk(self, logits, ld: Optional[int] = None, logprobs_out=None, lse_out=None, lse_in=None,
+                         stream=None) -> None:
+        ld = logits.stride(0) if ld is None else ld
+        check(lib().gr_constrained_topk(self.handle, logits.data_ptr(), ld, _ptr(logprobs_out), _ptr(lse_out),
+                                        _ptr(lse_in), _stream_ptr(stream)))
+
+    def advance(self, stream=None) -> None:
+        check(lib().gr_beam_advance(self.handle, _stream_ptr(stream)))
+
+    def rewind(self, step: int) -> None:
+        check(lib().gr_beam_rewind(self.handle, step))
+
+    # -- reading back ----------------------------------------------------------
+    def results(self, request: int, stream=None):
+        """(codes int32 [n, L], item_ids int64 [n], scores float32 [n])."""
+        W, L = self.widths[request], self.cfg.n_levels
+        codes = np.zeros((W, L), dtype=np.int32)
+        items = np.zeros(W, dtype=np.int64)
+        scores = np.zeros(W, dtype=np.float32)
+        n = ctypes.c_int()
+        check(lib().gr_beam_results(self.handle, request, codes.ctypes.data, items.ctypes.data,
+                                    scores.ctypes.data, ctypes.byref(n), _stream_ptr(stream)))
+        return codes[:n.value], items[:n.value], scores[:n.value]
+
+    def path(self, request: int, level: int, stream=None):
+        """BeamPath level: (parents, tokens, nodes, scores) of the beams it produced."""
+        W = self.widths[request]
+        par = np.zeros(W, dtype=np.int32)
+        tok = np.zeros(W, dtype=np.int32)
+        nod = np.zeros(W, dtype=np.int32)
+        sc = np.zeros(W, dtype=np.float32)
+        n = ctypes.c_int()
+        check(lib().gr_beam_path(self.handle, request, level, par.ctypes.data, tok.ctypes.data, nod.ctypes.data,
+                                 sc.ctypes.data, ctypes.byref(n), _stream_ptr(stream)))
+        k = n.value
+        return par[:k], tok[:k], nod[:k], sc[:k]
+
+    def status(self, clear: bool = False, stream=None) -> int:
+        """Device status as a gr_status code (does not raise)."""
+        return lib().gr_beam_status(self.handle, 1 if clear else 0, _stream_ptr(stream))
+
+    # -- measurement -----------------------------------------------------------------
+    def set_timing(self, enable: bool) -> None:
+        check(lib().gr_beam_set_timing(self.handle, 1 if enable else 0))
+
+    def kernel_stats(self, kind: int, reset: bool = False) -> Tuple[int, float]:
+        n = ctypes.c_int64()
+        ms = ctypes.c_double()
+        check(lib().gr_beam_kernel_stats(self.handle, kind, ctypes.byref(n), ctypes.byref(ms), 1 if reset else 0))
+        return n.value, ms.value
+
+    def set_wait_limit(self, ns: int) -> None:
+        check(lib().gr_beam_set_wait_limit(self.handle, ns))

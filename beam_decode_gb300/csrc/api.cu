@@ -1,0 +1,854 @@
+// Host side of libgrbeam: the C ABI declared in include/grbeam.h.
+//
+// The split KV layout (ContextKV shared per request, BeamKV per beam, BeamPath
+// ancestry), dynamic beam width and item-constrained top-K follow the zhiding.cn
+// recsys-examples article, section "语义ID生成式推荐专用推理框架"; returning
+// every beam follows "Advancing Generative Recommendation Inference: our
+// collaboration with NVIDIA on TensorRT LLM", section "Background: what
+// inference a recommendation request needs".  Beam search lives entirely on
+// the device: no call between create and results synchronises the host
+// (vLLM's out-of-engine, CPU-scheduled beam search is what the same page,
+// section "Why beam search could not saturate the GPU in vLLM", names as the
+// bottleneck).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "grbeam_internal.h"
+
+using namespace grb;
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+namespace {
+thread_local std::string g_last_error;
+
+gr_status fail(gr_status code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+gr_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(GR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define GR_CUDA(call, what)                            \
+    do {                                               \
+        cudaError_t e_ = (call);                       \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 3-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds
+gr_status make_tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+                       uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+    EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return fail(GR_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GR_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return GR_OK;
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// trie
+// ---------------------------------------------------------------------------
+struct gr_trie {
+    int n_levels = 0, C = 0, mask_words = 0;
+    int64_t n_items = 0, n_inner = 0, leaf_base = 0;
+    const uint32_t* mask = nullptr;
+    const int32_t* child_base = nullptr;
+    const int64_t* leaf_item = nullptr;
+};
+
+namespace {
+struct TrieLayout {
+    int64_t n_inner = 0, n_items = 0;
+    int mask_words = 0;
+    size_t off_mask = 0, off_child = 0, off_leaf = 0, total = 0;
+};
+
+gr_status check_items(const int32_t* codes, int64_t n_items, int n_levels, int C) {
+    if (codes == nullptr && n_items > 0) return fail(GR_ERR_INVALID_ARG, "codes is NULL");
+    if (n_items < 1) return fail(GR_ERR_INVALID_ARG, "n_items must be >= 1");
+    if (n_levels < 1 || n_levels > kMaxLevels) return fail(GR_ERR_UNSUPPORTED, "n_levels must be in 1..%d", kMaxLevels);
+    if (C < 1 || C > kMaxCodes) return fail(GR_ERR_UNSUPPORTED, "codes_per_level must be in 1..%d", kMaxCodes);
+    for (int64_t i = 0; i < n_items * n_levels; ++i)
+        if (codes[i] < 0 || codes[i] >= C)
+            return fail(GR_ERR_INVALID_ARG, "code %d of item %lld out of range", codes[i], (long long)(i / n_levels));
+    return GR_OK;
+}
+
+// sort item indices lexicographically by code tuple; count prefix nodes
+gr_status trie_order(const int32_t* codes, int64_t n, int L, std::vector<int64_t>& order,
+                     std::vector<int64_t>& level_nodes) {
+    order.resize(n);
+    for (int64_t i = 0; i < n; ++i) order[i] = i;
+    std::sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+        return std::lexicographical_compare(codes + a * L, codes + a * L + L, codes + b * L, codes + b * L + L);
+    });
+    for (int64_t i = 1; i < n; ++i)
+        if (std::equal(codes + order[i] * L, codes + order[i] * L + L, codes + order[i - 1] * L))
+            return fail(GR_ERR_INVALID_ARG, "duplicate item (items %lld and %lld have the same codes)",
+                        (long long)order[i - 1], (long long)order[i]);
+    // nodes at depth d (d = 0 root .. L leaves): distinct prefixes of length d
+    level_nodes.assign(L + 1, 0);
+    level_nodes[0] = 1;
+    for (int d = 1; d <= L; ++d) {
+        int64_t cnt = 0;
+        for (int64_t i = 0; i < n; ++i)
+            if (i == 0 || !std::equal(codes + order[i] * L, codes + order[i] * L + d, codes + order[i - 1] * L))
+                ++cnt;
+        level_nodes[d] = cnt;
+    }
+    return GR_OK;
+}
+
+TrieLayout trie_layout(const std::vector<int64_t>& level_nodes, int L, int C) {
+    TrieLayout t;
+    t.mask_words = (C + 31) / 32;
+    for (int d = 0; d < L; ++d) t.n_inner += level_nodes[d];
+    t.n_items = level_nodes[L];
+    t.off_mask = 0;
+    t.off_child = align_up(t.off_mask + (size_t)t.n_inner * t.mask_words * 4, 256);
+    t.off_leaf = align_up(t.off_child + (size_t)t.n_inner * 4, 256);
+    t.total = align_up(t.off_leaf + (size_t)t.n_items * 8, 256);
+    return t;
+}
+}  // namespace
+
+extern "C" gr_status gr_trie_device_bytes(const int32_t* codes, int64_t n_items, int n_levels, int codes_per_level,
+                                          size_t* bytes) {
+    if (bytes == nullptr) return fail(GR_ERR_INVALID_ARG, "bytes is NULL");
+    gr_status s = check_items(codes, n_items, n_levels, codes_per_level);
+    if (s != GR_OK) return s;
+    std::vector<int64_t> order, level_nodes;
+    try {
+        if ((s = trie_order(codes, n_items, n_levels, order, level_nodes)) != GR_OK) return s;
+    } catch (const std::bad_alloc&) {
+        return fail(GR_ERR_CAPACITY, "host allocation failed");
+    }
+    *bytes = trie_layout(level_nodes, n_levels, codes_per_level).total;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_trie_create(const int32_t* codes, const int64_t* item_ids, int64_t n_items, int n_levels,
+                                    int codes_per_level, void* dev_buf, size_t dev_bytes, gr_stream_t stream,
+                                    gr_trie** out) {
+    if (out == nullptr) return fail(GR_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    gr_status s = check_items(codes, n_items, n_levels, codes_per_level);
+    if (s != GR_OK) return s;
+    if (dev_buf == nullptr || (reinterpret_cast<uintptr_t>(dev_buf) & 255) != 0)
+        return fail(GR_ERR_INVALID_ARG, "dev_buf must be non-NULL and 256-byte aligned");
+    const int L = n_levels, C = codes_per_level;
+    try {
+        std::vector<int64_t> order, level_nodes;
+        if ((s = trie_order(codes, n_items, L, order, level_nodes)) != GR_OK) return s;
+        const TrieLayout lay = trie_layout(level_nodes, L, C);
+        if (dev_bytes < lay.total)
+            return fail(GR_ERR_CAPACITY, "trie needs %zu device bytes, got %zu", lay.total, dev_bytes);
+        std::vector<uint8_t> host(lay.total, 0);
+        uint32_t* mask = reinterpret_cast<uint32_t*>(host.data() + lay.off_mask);
+        int32_t* child = reinterpret_cast<int32_t*>(host.data() + lay.off_child);
+        int64_t* leaf = reinterpret_cast<int64_t*>(host.data() + lay.off_leaf);
+        // node ids: depth 0 (root) first, then depth 1, ..., leaves last
+        std::vector<int64_t> level_base(L + 1, 0);
+        for (int d = 1; d <= L; ++d) level_base[d] = level_base[d - 1] + level_nodes[d - 1];
+        if (level_base[L] + level_nodes[L] > INT32_MAX) return fail(GR_ERR_CAPACITY, "too many trie nodes");
+        // walk the sorted items once per depth: node id of each item's prefix.
+        // Children of one parent are contiguous in sorted order, numbered in
+        // code order, so child(node, c) = child_base[node] + rank of c in mask.
+        std::vector<int64_t> cur(n_items, 0), next(n_items, 0);
+        for (int d = 0; d < L; ++d) {
+            int64_t child_id = level_base[d + 1] - 1;
+            int64_t last_parent = -1;
+            for (int64_t k = 0; k < n_items; ++k) {
+                const int32_t* it = codes + order[k] * L;
+                const bool new_child = (k == 0) || !std::equal(it, it + d + 1, codes + order[k - 1] * L);
+                if (new_child) {
+                    ++child_id;
+                    const int64_t parent = cur[k];
+                    if (parent != last_parent) {
+                        child[parent] = (int32_t)child_id;
+                        last_parent = parent;
+                    }
+                    mask[(size_t)parent * lay.mask_words + (it[d] >> 5)] |= 1u << (it[d] & 31);
+                }
+                next[k] = child_id;
+            }
+            std::swap(cur, next);
+        }
+        for (int64_t k = 0; k < n_items; ++k)
+            leaf[cur[k] - level_base[L]] = item_ids ? item_ids[order[k]] : order[k];
+        GR_CUDA(cudaMemcpyAsync(dev_buf, host.data(), lay.total, cudaMemcpyHostToDevice, (cudaStream_t)stream),
+                "trie upload");
+        GR_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "trie upload sync");
+        gr_trie* t = new gr_trie;
+        t->n_levels = L;
+        t->C = C;
+        t->mask_words = lay.mask_words;
+        t->n_items = n_items;
+        t->n_inner = lay.n_inner;
+        t->leaf_base = level_base[L];
+        uint8_t* db = static_cast<uint8_t*>(dev_buf);
+        t->mask = reinterpret_cast<const uint32_t*>(db + lay.off_mask);
+        t->child_base = reinterpret_cast<const int32_t*>(db + lay.off_child);
+        t->leaf_item = reinterpret_cast<const int64_t*>(db + lay.off_leaf);
+        *out = t;
+    } catch (const std::bad_alloc&) {
+        return fail(GR_ERR_CAPACITY, "host allocation failed");
+    }
+    return GR_OK;
+}
+
+extern "C" gr_status gr_trie_destroy(gr_trie* trie) {
+    delete trie;
+    return GR_OK;
+}
+
+// ---------------------------------------------------------------------------
+// batch handle
+// ---------------------------------------------------------------------------
+namespace {
+struct Schedule {
+    std::vector<GrAttnUnit> units;
+    std::vector<GrAttnJob> jobs;
+    std::vector<int2> cta_jobs;
+};
+
+struct WsLayout {
+    size_t req, row_req, n_beams, parent, token, node, score, path, cand, sel_parent, sel_code, sel_key, n_sel,
+        status, tmaps, jobs, cta_jobs, units, tables_end, o_part, lse_part, res_codes, res_items, res_scores, total;
+};
+
+gr_status check_config(const gr_config* c, const gr_request* reqs, int n) {
+    if (c == nullptr || (reqs == nullptr && n > 0)) return fail(GR_ERR_INVALID_ARG, "NULL config or requests");
+    if (n < 1) return fail(GR_ERR_INVALID_ARG, "n_requests must be >= 1");
+    if (c->n_layers < 1) return fail(GR_ERR_INVALID_ARG, "n_layers must be >= 1");
+    if (c->n_kv_heads < 1 || c->n_q_heads < c->n_kv_heads || c->n_q_heads % c->n_kv_heads != 0)
+        return fail(GR_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+    const int G = c->n_q_heads / c->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+        return fail(GR_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4, 8 or 16 (got %d)", G);
+    if (c->head_dim != 64 && c->head_dim != 128) return fail(GR_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (c->n_levels < 1 || c->n_levels > kMaxLevels)
+        return fail(GR_ERR_UNSUPPORTED, "n_levels must be in 1..%d", kMaxLevels);
+    if (c->codes_per_level < 1 || c->codes_per_level > kMaxCodes)
+        return fail(GR_ERR_UNSUPPORTED, "codes_per_level must be in 1..%d", kMaxCodes);
+    if (c->vocab < 1 || c->code_base < 0 ||
+        (int64_t)c->code_base + (int64_t)c->n_levels * c->codes_per_level > c->vocab)
+        return fail(GR_ERR_INVALID_ARG, "code tokens [code_base, code_base + L*C) must lie inside the vocabulary");
+    if (c->pool_tokens < 1) return fail(GR_ERR_INVALID_ARG, "pool_tokens must be >= 1");
+    for (int r = 0; r < n; ++r) {
+        const gr_request& q = reqs[r];
+        if (q.ctx_len < 1 || q.ctx_offset < 0 || q.ctx_offset + q.ctx_len > c->pool_tokens)
+            return fail(GR_ERR_INVALID_ARG, "request %d: context [%lld, %lld) outside the pool", r,
+                        (long long)q.ctx_offset, (long long)(q.ctx_offset + q.ctx_len));
+        if (q.beam_width < 1 || q.beam_width > kMaxBeam)
+            return fail(GR_ERR_CAPACITY, "request %d: beam_width must be in 1..%d", r, kMaxBeam);
+        if (q.trie == nullptr) return fail(GR_ERR_INVALID_ARG, "request %d: trie is NULL", r);
+        if (q.trie->n_levels != c->n_levels || q.trie->C != c->codes_per_level)
+            return fail(GR_ERR_INVALID_ARG, "request %d: trie levels/codes do not match the config", r);
+    }
+    return GR_OK;
+}
+
+// Attention schedule: units of <= 256 query rows per (request, KV head);
+// their key tiles are cut into ~equal contiguous ranges, one per CTA.
+Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n_sm,
+                        std::vector<int>& unit_off, std::vector<int>& n_ub) {
+    Schedule s;
+    const int G = c->n_q_heads / c->n_kv_heads;
+    const int bpu = kUnitRows / G;
+    unit_off.resize(n);
+    n_ub.resize(n);
+    int64_t total = 0;
+    for (int r = 0; r < n; ++r) {
+        unit_off[r] = (int)s.units.size();
+        n_ub[r] = (reqs[r].beam_width + bpu - 1) / bpu;
+        const int tiles = (reqs[r].ctx_len + kTileKeys - 1) / kTileKeys;
+        for (int h = 0; h < c->n_kv_heads; ++h)
+            for (int ub = 0; ub < n_ub[r]; ++ub) {
+                GrAttnUnit u{};
+                u.req = r;
+                u.head = h;
+                u.beam0 = ub * bpu;
+                const int rows_left = (reqs[r].beam_width - u.beam0) * G;
+                u.nqt = rows_left > kTileRows ? 2 : 1;
+                u.n_tiles = tiles;
+                s.units.push_back(u);
+                total += (int64_t)tiles * u.nqt;
+            }
+    }
+    int64_t tiles_all = 0;
+    for (auto& u : s.units) tiles_all += u.n_tiles;
+    int n_cta = (int)std::min<int64_t>(std::max(n_sm, 1), tiles_all);
+    s.cta_jobs.resize(n_cta);
+    // walk units and tiles in order, cutting at cost boundaries
+    int cta = 0;
+    int64_t acc = 0;
+    int64_t bound = (total * (cta + 1) + n_cta - 1) / n_cta;
+    int job_begin = 0;
+    for (int ui = 0; ui < (int)s.units.size(); ++ui) {
+        GrAttnUnit& u = s.units[ui];
+        u.first_slot = (int)s.jobs.size();
+        int t0 = 0;
+        for (int t = 0; t < u.n_tiles; ++t) {
+            acc += u.nqt;
+            const bool last_tile = (t == u.n_tiles - 1);
+            const bool cut = acc >= bound && cta < n_cta - 1;
+            if (cut || last_tile) {
+                GrAttnJob j{ui, t0, t + 1, (int)s.jobs.size()};
+                s.jobs.push_back(j);
+                t0 = t + 1;
+            }
+            if (cut) {
+                s.cta_jobs[cta] = make_int2(job_begin, (int)s.jobs.size());
+                job_begin = (int)s.jobs.size();
+                ++cta;
+                bound = (total * (cta + 1) + n_cta - 1) / n_cta;
+            }
+        }
+        u.n_slots = (int)s.jobs.size() - u.first_slot;
+    }
+    s.cta_jobs[cta] = make_int2(job_begin, (int)s.jobs.size());
+    // CTAs that received no job (only possible when cuts ran ahead) get an empty range
+    for (int k = cta + 1; k < n_cta; ++k) s.cta_jobs[k] = make_int2((int)s.jobs.size(), (int)s.jobs.size());
+    return s;
+}
+
+WsLayout ws_layout(const gr_config* c, int n, int rows, const Schedule& s) {
+    WsLayout w{};
+    size_t o = 0;
+    auto take = [&](size_t bytes, size_t align = 256) {
+        o = align_up(o, align);
+        size_t r = o;
+        o += bytes;
+        return r;
+    };
+    const int L = c->n_levels;
+    // tables uploaded at create come first
+    w.req = take(sizeof(GrReqDev) * n);
+    w.row_req = take(4ull * rows);
+    w.tmaps = take(sizeof(CUtensorMap) * 2 * n, 128);
+    w.jobs = take(sizeof(GrAttnJob) * s.jobs.size());
+    w.cta_jobs = take(sizeof(int2) * s.cta_jobs.size());
+    w.units = take(sizeof(GrAttnUnit) * s.units.size());
+    w.tables_end = align_up(o, 256);
+    // device state
+    w.n_beams = take(4ull * n * (L + 1));
+    w.parent = take(4ull * L * rows);
+    w.token = take(4ull * L * rows);
+    w.node = take(4ull * L * rows);
+    w.score = take(4ull * L * rows);
+    w.path = take(4ull * L * rows * L);
+    w.cand = take(4ull * rows * c->codes_per_level);
+    w.sel_parent = take(4ull * rows);
+    w.sel_code = take(4ull * rows);
+    w.sel_key = take(4ull * rows);
+    w.n_sel = take(4ull * n);
+    w.status = take(16);
+    w.o_part = take(4ull * s.jobs.size() * kUnitRows * c->head_dim);
+    w.lse_part = take(4ull * s.jobs.size() * kUnitRows);
+    w.res_codes = take(4ull * rows * L);
+    w.res_items = take(8ull * rows);
+    w.res_scores = take(4ull * rows);
+    w.total = align_up(o, 256);
+    return w;
+}
+
+int rows_of(const gr_request* reqs, int n) {
+    int rows = 0;
+    for (int r = 0; r < n; ++r) rows += reqs[r].beam_width;
+    return rows;
+}
+}  // namespace
+
+struct gr_beam {
+    gr_config cfg{};
+    int n_req = 0, rows = 0;
+    std::vector<int> row_off;
+    std::vector<gr_request> reqs;
+    gr_buffers bufs{};
+    GrState st{};
+    Schedule sched;
+    int n_sm = 0;
+    // step state
+    int step = 0;
+    std::vector<uint8_t> attn_done;
+    bool topk_done = false;
+    // measurement
+    bool timing = false;
+    int64_t launches[GR_KERNEL_KINDS] = {};
+    struct Ev { cudaEvent_t a, b; };
+    std::vector<Ev> events[GR_KERNEL_KINDS];
+    std::vector<Ev> event_pool;
+    int64_t wait_limit_ns = 2000000000ll;
+
+    ~gr_beam() {
+        for (int k = 0; k < GR_KERNEL_KINDS; ++k)
+            for (auto& e : events[k]) event_pool.push_back(e);
+        for (auto& e : event_pool) {
+            cudaEventDestroy(e.a);
+            cudaEventDestroy(e.b);
+        }
+    }
+};
+
+namespace {
+// wrap one launch: count it, bracket it with events when timing is on
+template <typename F>
+gr_status run_kernel(gr_beam* h, int kind, cudaStream_t s, F&& launch) {
+    gr_beam::Ev ev{nullptr, nullptr};
+    if (h->timing) {
+        if (!h->event_pool.empty()) {
+            ev = h->event_pool.back();
+            h->event_pool.pop_back();
+        } else {
+            GR_CUDA(cudaEventCreate(&ev.a), "event create");
+            GR_CUDA(cudaEventCreate(&ev.b), "event create");
+        }
+        GR_CUDA(cudaEventRecord(ev.a, s), "event record");
+    }
+    cudaError_t e = launch();
+    if (e != cudaSuccess) {
+        if (ev.a) h->event_pool.push_back(ev);
+        return cuda_fail(e, "kernel launch");
+    }
+    ++h->launches[kind];
+    if (h->timing) {
+        GR_CUDA(cudaEventRecord(ev.b, s), "event record");
+        h->events[kind].push_back(ev);
+    }
+    return GR_OK;
+}
+
+gr_status status_from_word(int w) {
+    if (w & kStatusTimeout) return fail(GR_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", w);
+    if (w & (kStatusNanKey | kStatusBadNode)) return fail(GR_ERR_DEVICE, "a kernel flagged invalid data (status 0x%x)", w);
+    return GR_OK;
+}
+}  // namespace
+
+extern "C" gr_status gr_beam_workspace_bytes(const gr_config* cfg, const gr_request* reqs, int n_requests,
+                                             size_t* bytes) {
+    if (bytes == nullptr) return fail(GR_ERR_INVALID_ARG, "bytes is NULL");
+    gr_status s = check_config(cfg, reqs, n_requests);
+    if (s != GR_OK) return s;
+    int n_sm = device_sm_count();
+    if (n_sm <= 0) n_sm = 148;
+    std::vector<int> uo, nu;
+    Schedule sc = build_schedule(cfg, reqs, n_requests, n_sm, uo, nu);
+    *bytes = ws_layout(cfg, n_requests, rows_of(reqs, n_requests), sc).total;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_kv_bytes(const gr_config* cfg, const gr_request* reqs, int n_requests, size_t* bytes) {
+    if (bytes == nullptr) return fail(GR_ERR_INVALID_ARG, "bytes is NULL");
+    gr_status s = check_config(cfg, reqs, n_requests);
+    if (s != GR_OK) return s;
+    const int rows = rows_of(reqs, n_requests);
+    *bytes = (size_t)cfg->n_layers * std::max(cfg->n_levels - 1, 0) * rows * cfg->n_kv_heads * cfg->head_dim * 2;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs, int n_requests,
+                                    const gr_buffers* bufs, gr_stream_t stream, gr_beam** out) {
+    if (out == nullptr || bufs == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL out or buffers");
+    *out = nullptr;
+    gr_status s = check_config(cfg, reqs, n_requests);
+    if (s != GR_OK) return s;
+    if (bufs->ctx_k == nullptr || bufs->ctx_v == nullptr || bufs->workspace == nullptr)
+        return fail(GR_ERR_INVALID_ARG, "ctx_k, ctx_v and workspace must be device pointers");
+    if (cfg->n_levels > 1 && (bufs->beam_k == nullptr || bufs->beam_v == nullptr))
+        return fail(GR_ERR_INVALID_ARG, "beam_k / beam_v are required when n_levels > 1");
+    if ((reinterpret_cast<uintptr_t>(bufs->workspace) & 255) != 0)
+        return fail(GR_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(bufs->ctx_k) & 15) != 0 || (reinterpret_cast<uintptr_t>(bufs->ctx_v) & 15) != 0)
+        return fail(GR_ERR_INVALID_ARG, "ctx_k / ctx_v must be 16-byte aligned");
+    const int n_sm = device_sm_count();
+    if (n_sm <= 0) return fail(GR_ERR_CUDA, "no CUDA device");
+    cudaStream_t cs = (cudaStream_t)stream;
+    gr_beam* h = nullptr;
+    try {
+        h = new gr_beam;
+        h->cfg = *cfg;
+        h->n_req = n_requests;
+        h->reqs.assign(reqs, reqs + n_requests);
+        h->bufs = *bufs;
+        h->n_sm = n_sm;
+        h->rows = rows_of(reqs, n_requests);
+        h->row_off.resize(n_requests + 1);
+        h->row_off[0] = 0;
+        for (int r = 0; r < n_requests; ++r) h->row_off[r + 1] = h->row_off[r] + reqs[r].beam_width;
+        std::vector<int> unit_off, n_ub;
+        h->sched = build_schedule(cfg, reqs, n_requests, n_sm, unit_off, n_ub);
+        const WsLayout w = ws_layout(cfg, n_requests, h->rows, h->sched);
+        if (bufs->workspace_bytes < w.total) {
+            gr_status e = fail(GR_ERR_CAPACITY, "workspace needs %zu bytes, got %zu", w.total, bufs->workspace_bytes);
+            delete h;
+            return e;
+        }
+        uint8_t* ws = static_cast<uint8_t*>(bufs->workspace);
+        GrState& st = h->st;
+        st.req = reinterpret_cast<GrReqDev*>(ws + w.req);
+        st.n_req = n_requests;
+        st.rows = h->rows;
+        st.n_levels = cfg->n_levels;
+        st.C = cfg->codes_per_level;
+        st.code_base = cfg->code_base;
+        st.vocab = cfg->vocab;
+        st.n_layers = cfg->n_layers;
+        st.n_q_heads = cfg->n_q_heads;
+        st.n_kv_heads = cfg->n_kv_heads;
+        st.head_dim = cfg->head_dim;
+        st.pool_tokens = cfg->pool_tokens;
+        st.row_req = reinterpret_cast<int32_t*>(ws + w.row_req);
+        st.n_beams = reinterpret_cast<int32_t*>(ws + w.n_beams);
+        st.parent = reinterpret_cast<int32_t*>(ws + w.parent);
+        st.token = reinterpret_cast<int32_t*>(ws + w.token);
+        st.node = reinterpret_cast<int32_t*>(ws + w.node);
+        st.score = reinterpret_cast<float*>(ws + w.score);
+        st.path = reinterpret_cast<int32_t*>(ws + w.path);
+        st.cand = reinterpret_cast<uint32_t*>(ws + w.cand);
+        st.sel_parent = reinterpret_cast<int32_t*>(ws + w.sel_parent);
+        st.sel_code = reinterpret_cast<int32_t*>(ws + w.sel_code);
+        st.sel_key = reinterpret_cast<float*>(ws + w.sel_key);
+        st.n_sel = reinterpret_cast<int32_t*>(ws + w.n_sel);
+        st.status = reinterpret_cast<int32_t*>(ws + w.status);
+        st.tmaps = reinterpret_cast<CUtensorMap*>(ws + w.tmaps);
+        st.jobs = reinterpret_cast<GrAttnJob*>(ws + w.jobs);
+        st.cta_jobs = reinterpret_cast<int2*>(ws + w.cta_jobs);
+        st.units = reinterpret_cast<GrAttnUnit*>(ws + w.units);
+        st.n_units = (int)h->sched.units.size();
+        st.n_jobs = (int)h->sched.jobs.size();
+        st.n_cta = (int)h->sched.cta_jobs.size();
+        st.o_part = reinterpret_cast<float*>(ws + w.o_part);
+        st.lse_part = reinterpret_cast<float*>(ws + w.lse_part);
+        st.beam_k = static_cast<const uint16_t*>(bufs->beam_k);
+        st.beam_v = static_cast<const uint16_t*>(bufs->beam_v);
+        st.res_codes = reinterpret_cast<int32_t*>(ws + w.res_codes);
+        st.res_items = reinterpret_cast<int64_t*>(ws + w.res_items);
+        st.res_scores = reinterpret_cast<float*>(ws + w.res_scores);
+
+        // host images of the device tables, uploaded with one copy
+        std::vector<uint8_t> img(w.tables_end, 0);
+        GrReqDev* rq = reinterpret_cast<GrReqDev*>(img.data() + w.req);
+        int32_t* rr = reinterpret_cast<int32_t*>(img.data() + w.row_req);
+        for (int r = 0; r < n_requests; ++r) {
+            const gr_trie* t = reqs[r].trie;
+            GrReqDev d{};
+            d.row_off = h->row_off[r];
+            d.width = reqs[r].beam_width;
+            d.ctx_len = reqs[r].ctx_len;
+            d.n_levels = t->n_levels;
+            d.unit_off = unit_off[r];
+            d.n_ub = n_ub[r];
+            d.mask_words = t->mask_words;
+            d.ctx_off = reqs[r].ctx_offset;
+            d.leaf_base = t->leaf_base;
+            d.n_nodes = t->n_inner;
+            d.mask = t->mask;
+            d.child_base = t->child_base;
+            d.leaf_item = t->leaf_item;
+            rq[r] = d;
+            for (int b = 0; b < reqs[r].beam_width; ++b) rr[h->row_off[r] + b] = r;
+        }
+        CUtensorMap* tm = reinterpret_cast<CUtensorMap*>(img.data() + w.tmaps);
+        const int D = cfg->head_dim;
+        const uint64_t zdim = (uint64_t)cfg->n_layers * cfg->n_kv_heads;
+        for (int r = 0; r < n_requests; ++r) {
+            const uint64_t off = (uint64_t)reqs[r].ctx_offset * D * 2;
+            const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)cfg->pool_tokens * D * 2;
+            if ((s = make_tmap_3d(&tm[2 * r], static_cast<const uint8_t*>(bufs->ctx_k) + off, D, reqs[r].ctx_len,
+                                  zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK ||
+                (s = make_tmap_3d(&tm[2 * r + 1], static_cast<const uint8_t*>(bufs->ctx_v) + off, D, reqs[r].ctx_len,
+                                  zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK) {
+                delete h;
+                return s;
+            }
+        }
+        memcpy(img.data() + w.jobs, h->sched.jobs.data(), sizeof(GrAttnJob) * h->sched.jobs.size());
+        memcpy(img.data() + w.cta_jobs, h->sched.cta_jobs.data(), sizeof(int2) * h->sched.cta_jobs.size());
+        memcpy(img.data() + w.units, h->sched.units.data(), sizeof(GrAttnUnit) * h->sched.units.size());
+        cudaError_t e = cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = launch_init_state(st, cs);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);  // img is released on return
+        if (e != cudaSuccess) {
+            delete h;
+            return cuda_fail(e, "workspace upload");
+        }
+        h->launches[GR_KERNEL_INIT] += 1;
+        h->attn_done.assign(cfg->n_layers, 0);
+    } catch (const std::bad_alloc&) {
+        delete h;
+        return fail(GR_ERR_CAPACITY, "host allocation failed");
+    }
+    *out = h;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_destroy(gr_beam* beam) {
+    delete beam;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_rows(const gr_beam* h, int* rows_total, int* row_offsets) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    if (rows_total) *rows_total = h->rows;
+    if (row_offsets)
+        for (int r = 0; r <= h->n_req; ++r) row_offsets[r] = h->row_off[r];
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_step(const gr_beam* h, int* step) {
+    if (h == nullptr || step == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    *step = h->step;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_kv_slot(gr_beam* h, int layer, void** k_new, void** v_new) {
+    if (h == nullptr || k_new == nullptr || v_new == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (layer < 0 || layer >= h->cfg.n_layers) return fail(GR_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (h->step < 1 || h->step >= h->cfg.n_levels)
+        return fail(GR_ERR_STATE, "no BeamKV level is open at step %d", h->step);
+    const gr_config& c = h->cfg;
+    const size_t off = (((size_t)layer * (c.n_levels - 1) + (h->step - 1)) * h->rows) * c.n_kv_heads * c.head_dim * 2;
+    *k_new = static_cast<uint8_t*>(h->bufs.beam_k) + off;
+    *v_new = static_cast<uint8_t*>(h->bufs.beam_v) + off;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_decode_attn(gr_beam* h, int layer, const void* q, void* out, gr_stream_t stream) {
+    if (h == nullptr || q == nullptr || out == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (layer < 0 || layer >= h->cfg.n_layers) return fail(GR_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if ((reinterpret_cast<uintptr_t>(q) & 15) != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0)
+        return fail(GR_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+    if (h->step < 1 || h->step >= h->cfg.n_levels)
+        return fail(GR_ERR_STATE, "attention runs at steps 1..%d (current step %d)", h->cfg.n_levels - 1, h->step);
+    if (h->topk_done) return fail(GR_ERR_STATE, "top-K of this step already ran; call gr_beam_advance");
+    if (h->attn_done[layer]) return fail(GR_ERR_STATE, "layer %d already ran at step %d", layer, h->step);
+    const gr_config& c = h->cfg;
+    const int G = c.n_q_heads / c.n_kv_heads;
+    CUtensorMap qmap;
+    gr_status s = make_tmap_3d(&qmap, q, c.head_dim, c.n_q_heads, h->rows, (uint64_t)c.head_dim * 2,
+                               (uint64_t)c.n_q_heads * c.head_dim * 2, 64, G, kTileRows / G);
+    if (s != GR_OK) return s;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const int64_t lim = h->wait_limit_ns;
+    if ((s = run_kernel(h, GR_KERNEL_CTX_ATTN, cs, [&] { return launch_ctx_attn(h->st, qmap, layer, lim, cs); })) !=
+        GR_OK)
+        return s;
+    const int t = h->step;
+    if ((s = run_kernel(h, GR_KERNEL_BEAM_ATTN, cs, [&] {
+             return launch_beam_attn(h->st, t, layer, static_cast<const uint16_t*>(q), static_cast<uint16_t*>(out), cs);
+         })) != GR_OK)
+        return s;
+    h->attn_done[layer] = 1;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_constrained_topk(gr_beam* h, const float* logits, int64_t ld, float* logprobs_out,
+                                         float* lse_out, const float* lse_in, gr_stream_t stream) {
+    if (h == nullptr || logits == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (ld < h->cfg.vocab || ld % 4 != 0) return fail(GR_ERR_INVALID_ARG, "ld must be >= vocab and a multiple of 4");
+    if ((reinterpret_cast<uintptr_t>(logits) & 15) != 0) return fail(GR_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+    if (h->step >= h->cfg.n_levels) return fail(GR_ERR_STATE, "decoding is finished");
+    if (h->topk_done) return fail(GR_ERR_STATE, "top-K already ran at step %d; call gr_beam_advance", h->step);
+    cudaStream_t cs = (cudaStream_t)stream;
+    const int t = h->step;
+    gr_status s;
+    if ((s = run_kernel(h, GR_KERNEL_LOGSOFTMAX, cs, [&] {
+             return launch_logsoftmax_gather(h->st, t, logits, ld, logprobs_out, lse_out, lse_in, cs);
+         })) != GR_OK)
+        return s;
+    if ((s = run_kernel(h, GR_KERNEL_TOPK, cs, [&] { return launch_topk_select(h->st, t, cs); })) != GR_OK) return s;
+    h->topk_done = true;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_advance(gr_beam* h, gr_stream_t stream) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    if (!h->topk_done) return fail(GR_ERR_STATE, "gr_constrained_topk has not run at step %d", h->step);
+    cudaStream_t cs = (cudaStream_t)stream;
+    const int t = h->step;
+    gr_status s = run_kernel(h, GR_KERNEL_ADVANCE, cs, [&] { return launch_advance(h->st, t, cs); });
+    if (s != GR_OK) return s;
+    h->step = t + 1;
+    h->topk_done = false;
+    std::fill(h->attn_done.begin(), h->attn_done.end(), 0);
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_rewind(gr_beam* h, int step) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    if (step < 1 || step > h->step)
+        return fail(GR_ERR_STATE, "can rewind only to a decoded step 1..%d (asked %d)", h->step, step);
+    h->step = step;
+    h->topk_done = false;
+    std::fill(h->attn_done.begin(), h->attn_done.end(), 0);
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_status(gr_beam* h, int clear_flag, gr_stream_t stream) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    cudaStream_t cs = (cudaStream_t)stream;
+    int w = 0;
+    GR_CUDA(cudaMemcpyAsync(&w, h->st.status, 4, cudaMemcpyDeviceToHost, cs), "status read");
+    GR_CUDA(cudaStreamSynchronize(cs), "status sync");
+    if (clear_flag && w != 0) {
+        GR_CUDA(cudaMemsetAsync(h->st.status, 0, 16, cs), "status clear");
+        GR_CUDA(cudaStreamSynchronize(cs), "status clear sync");
+    }
+    return status_from_word(w);
+}
+
+extern "C" gr_status gr_beam_results(gr_beam* h, int request, int32_t* codes, int64_t* item_ids, float* scores,
+                                     int* n_out, gr_stream_t stream) {
+    if (h == nullptr || n_out == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (request < 0 || request >= h->n_req) return fail(GR_ERR_INVALID_ARG, "request %d out of range", request);
+    if (h->step < h->cfg.n_levels) return fail(GR_ERR_STATE, "decoding is not finished (step %d of %d)", h->step,
+                                               h->cfg.n_levels);
+    cudaStream_t cs = (cudaStream_t)stream;
+    gr_status s = run_kernel(h, GR_KERNEL_RESULTS, cs, [&] { return launch_results(h->st, cs); });
+    if (s != GR_OK) return s;
+    const int L = h->cfg.n_levels;
+    int n = 0, w = 0;
+    GR_CUDA(cudaMemcpyAsync(&n, h->st.n_beams + request * (L + 1) + L, 4, cudaMemcpyDeviceToHost, cs), "results");
+    GR_CUDA(cudaMemcpyAsync(&w, h->st.status, 4, cudaMemcpyDeviceToHost, cs), "status read");
+    GR_CUDA(cudaStreamSynchronize(cs), "results sync");
+    if ((s = status_from_word(w)) != GR_OK) return s;
+    const int row0 = h->row_off[request];
+    if (n > 0) {
+        if (codes)
+            GR_CUDA(cudaMemcpyAsync(codes, h->st.res_codes + (size_t)row0 * L, 4ull * n * L, cudaMemcpyDeviceToHost, cs),
+                    "results");
+        if (item_ids)
+            GR_CUDA(cudaMemcpyAsync(item_ids, h->st.res_items + row0, 8ull * n, cudaMemcpyDeviceToHost, cs), "results");
+        if (scores)
+            GR_CUDA(cudaMemcpyAsync(scores, h->st.res_scores + row0, 4ull * n, cudaMemcpyDeviceToHost, cs), "results");
+        GR_CUDA(cudaStreamSynchronize(cs), "results sync");
+    }
+    *n_out = n;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_path(gr_beam* h, int request, int level, int32_t* parents, int32_t* tokens,
+                                  int32_t* nodes, float* scores, int* n_out, gr_stream_t stream) {
+    if (h == nullptr || n_out == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (request < 0 || request >= h->n_req) return fail(GR_ERR_INVALID_ARG, "request %d out of range", request);
+    if (level < 0 || level >= h->step) return fail(GR_ERR_STATE, "level %d is not committed (step %d)", level, h->step);
+    cudaStream_t cs = (cudaStream_t)stream;
+    const int L = h->cfg.n_levels;
+    int n = 0, w = 0;
+    GR_CUDA(cudaMemcpyAsync(&n, h->st.n_beams + request * (L + 1) + level + 1, 4, cudaMemcpyDeviceToHost, cs), "path");
+    GR_CUDA(cudaMemcpyAsync(&w, h->st.status, 4, cudaMemcpyDeviceToHost, cs), "status read");
+    GR_CUDA(cudaStreamSynchronize(cs), "path sync");
+    gr_status s = status_from_word(w);
+    if (s != GR_OK) return s;
+    const size_t base = (size_t)level * h->rows + h->row_off[request];
+    if (n > 0) {
+        if (parents) GR_CUDA(cudaMemcpyAsync(parents, h->st.parent + base, 4ull * n, cudaMemcpyDeviceToHost, cs), "path");
+        if (tokens) GR_CUDA(cudaMemcpyAsync(tokens, h->st.token + base, 4ull * n, cudaMemcpyDeviceToHost, cs), "path");
+        if (nodes) GR_CUDA(cudaMemcpyAsync(nodes, h->st.node + base, 4ull * n, cudaMemcpyDeviceToHost, cs), "path");
+        if (scores) GR_CUDA(cudaMemcpyAsync(scores, h->st.score + base, 4ull * n, cudaMemcpyDeviceToHost, cs), "path");
+        GR_CUDA(cudaStreamSynchronize(cs), "path sync");
+    }
+    *n_out = n;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_set_timing(gr_beam* h, int enable) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    h->timing = enable != 0;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_kernel_stats(gr_beam* h, int kind, int64_t* launches, double* total_ms, int reset) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    if (kind < 0 || kind >= GR_KERNEL_KINDS) return fail(GR_ERR_INVALID_ARG, "kernel kind %d out of range", kind);
+    if (launches) *launches = h->launches[kind];
+    double ms = 0.0;
+    for (auto& e : h->events[kind]) {
+        GR_CUDA(cudaEventSynchronize(e.b), "event sync");
+        float f = 0.f;
+        GR_CUDA(cudaEventElapsedTime(&f, e.a, e.b), "event elapsed");
+        ms += f;
+    }
+    if (total_ms) *total_ms = ms;
+    if (reset) {
+        h->launches[kind] = 0;
+        for (auto& e : h->events[kind]) h->event_pool.push_back(e);
+        h->events[kind].clear();
+    }
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_set_wait_limit(gr_beam* h, int64_t nanoseconds) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    h->wait_limit_ns = (nanoseconds == 0) ? 2000000000ll : nanoseconds;
+    return GR_OK;
+}
+
+extern "C" const char* gr_status_str(gr_status s) {
+    switch (s) {
+        case GR_OK: return "GR_OK";
+        case GR_ERR_INVALID_ARG: return "GR_ERR_INVALID_ARG";
+        case GR_ERR_UNSUPPORTED: return "GR_ERR_UNSUPPORTED";
+        case GR_ERR_CAPACITY: return "GR_ERR_CAPACITY";
+        case GR_ERR_STATE: return "GR_ERR_STATE";
+        case GR_ERR_CUDA: return "GR_ERR_CUDA";
+        case GR_ERR_TIMEOUT: return "GR_ERR_TIMEOUT";
+        case GR_ERR_DEVICE: return "GR_ERR_DEVICE";
+        default: return "unknown gr_status";
+    }
+}
+
+extern "C" const char* gr_last_error(void) { return g_last_error.c_str(); }

@@ -1,0 +1,123 @@
+// Internal layout shared by the host library and the kernels of libgrbeam.
+//
+// Everything here lives in the caller's workspace (device memory) and is
+// described by GrState, which every kernel receives by value.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/grbeam.h"
+
+namespace grb {
+
+constexpr int kMaxBeam = 1024;        // W_r upper bound (one CTA of the selection kernel)
+constexpr int kMaxCodes = 1024;       // C upper bound
+constexpr int kMaxLevels = 8;         // L upper bound
+constexpr int kTileRows = 128;        // query rows per tensor-core tile (TMEM lanes)
+constexpr int kTileKeys = 128;        // context keys per tile
+constexpr int kUnitRows = 256;        // query rows per attention unit (two tiles)
+constexpr int kLogitCluster = 4;      // CTAs sharing one logit row
+
+// status word bits (device)
+constexpr int kStatusNanKey = 1;      // a candidate key was NaN
+constexpr int kStatusTimeout = 2;     // a pipeline wait gave up
+constexpr int kStatusBadNode = 4;     // trie walk left the valid node range
+
+// Per-request record (device copy).
+struct GrReqDev {
+    int row_off;        // first row of the request
+    int width;          // W_r
+    int ctx_len;        // T_r
+    int n_levels;       // L_r (== cfg.n_levels)
+    int unit_off;       // first attention unit of the request
+    int n_ub;           // units per KV head: ceil(W_r * G / kUnitRows)
+    int mask_words;     // 32-bit words per trie node mask
+    int pad0;
+    int64_t ctx_off;    // first token in the ContextKV pool
+    int64_t leaf_base;  // node id of the first leaf
+    int64_t n_nodes;    // inner nodes
+    const uint32_t* mask;      // [n_inner][mask_words]
+    const int32_t* child_base; // [n_inner]
+    const int64_t* leaf_item;  // [n_items]
+};
+
+// One piece of attention work: key tiles [t0, t1) of one unit.
+struct GrAttnJob {
+    int unit;
+    int t0, t1;
+    int slot;           // partial-result slot (== job index)
+};
+
+// A unit: up to two 128-row query tiles of one (request, KV head).
+struct GrAttnUnit {
+    int req;
+    int head;           // KV head
+    int beam0;          // first beam of the unit
+    int nqt;            // query tiles (1 or 2)
+    int first_slot;     // jobs of the unit are slots [first_slot, first_slot + n_slots)
+    int n_slots;
+    int n_tiles;        // ceil(T_r / kTileKeys)
+    int pad;
+};
+
+struct GrState {
+    GrReqDev* req;
+    int n_req;
+    int rows;           // sum of W_r
+    int n_levels;       // L
+    int C;              // codes per level
+    int code_base;
+    int vocab;
+    int n_layers, n_q_heads, n_kv_heads, head_dim;
+    int64_t pool_tokens;
+
+    int32_t* row_req;   // [rows] request of each row
+    int32_t* n_beams;   // [n_req][L+1] live beams entering step t
+    int32_t* parent;    // [L][rows] BeamPath: parent slot at level t-1
+    int32_t* token;     // [L][rows]
+    int32_t* node;      // [L][rows] trie node after consuming the level's code
+    float* score;       // [L][rows]
+    int32_t* path;      // [L][rows][L] slots on the path, levels 0..t
+    uint32_t* cand;     // [rows][C] ordered candidate keys (0 = not a candidate)
+    int32_t* sel_parent;// [rows] selection of the current step (request-relative rank)
+    int32_t* sel_code;  // [rows]
+    float* sel_key;     // [rows]
+    int32_t* n_sel;     // [n_req]
+    int32_t* status;    // [4]
+
+    // attention
+    CUtensorMap* tmaps; // [n_req][2] (K, V) of the ContextKV pool
+    GrAttnJob* jobs;    // [n_jobs]
+    int2* cta_jobs;     // [n_cta] job range of each CTA
+    GrAttnUnit* units;  // [n_units]
+    int n_units, n_jobs, n_cta;
+    float* o_part;      // [n_jobs][kUnitRows][D]
+    float* lse_part;    // [n_jobs][kUnitRows]
+    const uint16_t* beam_k; // bf16 [NL][L-1][rows][Hkv][D]
+    const uint16_t* beam_v;
+
+    // results staging
+    int32_t* res_codes; // [rows][L]
+    int64_t* res_items; // [rows]
+    float* res_scores;  // [rows]
+};
+
+// ---- launchers (k_topk.cu) ----
+cudaError_t launch_init_state(const GrState& st, cudaStream_t s);
+cudaError_t launch_logsoftmax_gather(const GrState& st, int t, const float* logits, int64_t ld,
+                                     float* logprobs_out, float* lse_out, const float* lse_in,
+                                     cudaStream_t s);
+cudaError_t launch_topk_select(const GrState& st, int t, cudaStream_t s);
+cudaError_t launch_advance(const GrState& st, int t, cudaStream_t s);
+cudaError_t launch_results(const GrState& st, cudaStream_t s);
+
+// ---- launchers (k_attn.cu) ----
+cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes);
+cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer,
+                            int64_t wait_limit_ns, cudaStream_t s);
+cudaError_t launch_beam_attn(const GrState& st, int t, int layer, const uint16_t* q, uint16_t* out,
+                             cudaStream_t s);
+
+}  // namespace grb

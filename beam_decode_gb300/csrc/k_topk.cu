@@ -1,0 +1,445 @@
+// Log-softmax, item-constrained top-K, BeamPath advance and results.
+//
+// The output logits give the ranking (zhiding.cn recsys-examples article,
+// section "语义ID：解决稀疏性与长尾问题"); the runtime keeps item-constrained
+// top-K, dynamic beam width and BeamPath (section "语义ID生成式推荐专用推理框架");
+// every surviving beam is returned ("Advancing Generative Recommendation
+// Inference: our collaboration with NVIDIA on TensorRT LLM", section
+// "Background: what inference a recommendation request needs").
+//
+// Kernels
+//   k_logsoftmax_gather  one pass over each live logit row (a cluster of 4 CTAs
+//                        per row): log-sum-exp of the full vocabulary, then the
+//                        level's C code logits -> masked float32 keys
+//                        key = S_b + (x - LSE_b), stored as order-preserving
+//                        uint32 (0 = not a candidate).  HBM-bound.
+//   k_topk_select        per request: radix select of the W-th largest key over
+//                        n_live*C candidates (12/12/8-bit digits), ties at the
+//                        threshold taken in flat-index order, then a bitonic
+//                        sort of the survivors by (key desc, flat asc).
+//   k_advance            BeamPath commit: parent, token, trie node, score,
+//                        ancestry row; sets the next step's live width.  No KV
+//                        is moved: later steps reach a beam's BeamKV slots
+//                        through its ancestry row.
+//   k_results            code strings, item ids and scores of the final beams.
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "grbeam_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace grb {
+namespace {
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float unorder_key(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// (m, s) pair: running maximum and sum of exp(x - m)
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+    if (m2 > m) {
+        s = s * exp2f((m - m2) * CUDART_L2E_F) + s2;
+        m = m2;
+    } else if (m2 > -CUDART_INF_F) {
+        s = s + s2 * exp2f((m2 - m) * CUDART_L2E_F);
+    }
+}
+
+__device__ __forceinline__ bool row_live(const GrState& st, int row, int t, int& r, int& b) {
+    r = st.row_req[row];
+    const GrReqDev& R = st.req[r];
+    b = row - R.row_off;
+    if (t >= R.n_levels) return false;
+    return b < st.n_beams[r * (st.n_levels + 1) + t];
+}
+
+// ---------------------------------------------------------------------------
+// K3: fused full-vocabulary log-softmax + level gather + trie mask
+// ---------------------------------------------------------------------------
+constexpr int kLsThreads = 256;
+
+__global__ void __cluster_dims__(kLogitCluster, 1, 1) __launch_bounds__(kLsThreads)
+k_logsoftmax_gather(GrState st, int t, const float* __restrict__ logits, int64_t ld,
+                    float* __restrict__ logprobs_out, float* __restrict__ lse_out,
+                    const float* __restrict__ lse_in) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int row = blockIdx.x / kLogitCluster;
+    const int part = (int)cluster.block_rank();
+    int r, b;
+    if (!row_live(st, row, t, r, b)) return;  // uniform over the cluster
+
+    __shared__ float red_m[kLsThreads / 32], red_s[kLsThreads / 32];
+    __shared__ float part_ms[2];
+
+    const float* x = logits + (int64_t)row * ld;
+    const int V = st.vocab;
+    float lse;
+    if (lse_in == nullptr) {
+        const int n4 = V >> 2;
+        const int b0 = (int)((int64_t)n4 * part / kLogitCluster);
+        const int b1 = (int)((int64_t)n4 * (part + 1) / kLogitCluster);
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        float m = -CUDART_INF_F, s = 0.f;
+        int i = b0 + threadIdx.x;
+        // 4 independent 16-byte loads in flight per thread
+        for (; i + 3 * kLsThreads < b1; i += 4 * kLsThreads) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldcs(x4 + i + u * kLsThreads);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float cm = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
+                if (cm > m) { s *= exp2f((m - cm) * CUDART_L2E_F); m = cm; }
+                const float ml = m * CUDART_L2E_F;
+                s += exp2f(fmaf(v[u].x, CUDART_L2E_F, -ml)) + exp2f(fmaf(v[u].y, CUDART_L2E_F, -ml)) +
+                     exp2f(fmaf(v[u].z, CUDART_L2E_F, -ml)) + exp2f(fmaf(v[u].w, CUDART_L2E_F, -ml));
+            }
+        }
+        for (; i < b1; i += kLsThreads) {
+            float4 v = __ldcs(x4 + i);
+            float cm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+            if (cm > m) { s *= exp2f((m - cm) * CUDART_L2E_F); m = cm; }
+            const float ml = m * CUDART_L2E_F;
+            s += exp2f(fmaf(v.x, CUDART_L2E_F, -ml)) + exp2f(fmaf(v.y, CUDART_L2E_F, -ml)) +
+                 exp2f(fmaf(v.z, CUDART_L2E_F, -ml)) + exp2f(fmaf(v.w, CUDART_L2E_F, -ml));
+        }
+        if (part == kLogitCluster - 1) {  // ragged tail of a row whose length is not a multiple of 4
+            for (int j = (n4 << 2) + threadIdx.x; j < V; j += kLsThreads) {
+                float v = x[j];
+                lse_merge(m, s, v, 1.f);
+            }
+        }
+        // warp, then block
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+            float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+            lse_merge(m, s, m2, s2);
+        }
+        const int w = threadIdx.x >> 5;
+        if ((threadIdx.x & 31) == 0) { red_m[w] = m; red_s[w] = s; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float mm = red_m[0], ss = red_s[0];
+            for (int k = 1; k < kLsThreads / 32; ++k) lse_merge(mm, ss, red_m[k], red_s[k]);
+            part_ms[0] = mm;
+            part_ms[1] = ss;
+        }
+        cluster.sync();
+        // every CTA combines the four partials in the same order
+        float mm = -CUDART_INF_F, ss = 0.f;
+        for (int k = 0; k < kLogitCluster; ++k) {
+            const float* pk = cluster.map_shared_rank(part_ms, k);
+            lse_merge(mm, ss, pk[0], pk[1]);
+        }
+        lse = mm + logf(ss);
+        cluster.sync();  // keep every CTA's shared memory alive until all have read it
+    } else {
+        lse = lse_in[row];
+    }
+    if (part == 0 && threadIdx.x == 0 && lse_out != nullptr) lse_out[row] = lse;
+
+    // level gather of C codes, split over the cluster
+    const GrReqDev& R = st.req[r];
+    const int C = st.C;
+    const int64_t node = (t == 0) ? 0 : st.node[(int64_t)(t - 1) * st.rows + row];
+    const float S = (t == 0) ? 0.f : st.score[(int64_t)(t - 1) * st.rows + row];
+    if (node < 0 || node >= R.n_nodes) {
+        if (threadIdx.x == 0 && part == 0) atomicOr(st.status, kStatusBadNode);
+        return;
+    }
+    const uint32_t* mk = R.mask + node * R.mask_words;
+    const float* xc = x + st.code_base + (int64_t)t * C;
+    uint32_t* out = st.cand + (int64_t)row * C;
+    const int c0 = (int)((int64_t)C * part / kLogitCluster);
+    const int c1 = (int)((int64_t)C * (part + 1) / kLogitCluster);
+    for (int c = c0 + threadIdx.x; c < c1; c += kLsThreads) {
+        const bool valid = (mk[c >> 5] >> (c & 31)) & 1u;
+        const float xv = xc[c];
+        const float lp = __fsub_rn(xv, lse);
+        float key = __fadd_rn(S, lp);
+        uint32_t u = 0;
+        if (valid) {
+            if (key != key) {
+                atomicOr(st.status, kStatusNanKey);
+            } else {
+                if (key == 0.f) key = 0.f;  // -0.0 -> +0.0
+                u = order_key(key);
+            }
+        }
+        out[c] = u;
+        if (logprobs_out != nullptr) logprobs_out[(int64_t)row * C + c] = valid ? lp : -CUDART_INF_F;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K4: cross-beam top-K of one request
+// ---------------------------------------------------------------------------
+constexpr int kSelThreads = 1024;
+constexpr int kHistBins = 4096;
+
+// inclusive prefix sum over the block in thread order; returns the block total
+__device__ __forceinline__ int block_incl_scan(int v, int* warp_tot, int& total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += y;
+    }
+    if (lane == 31) warp_tot[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int tv = (lane < (kSelThreads >> 5)) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, tv, off);
+            if (lane >= off) tv += y;
+        }
+        warp_tot[lane] = tv;  // inclusive warp prefix
+    }
+    __syncthreads();
+    const int add = (w > 0) ? warp_tot[w - 1] : 0;
+    total = warp_tot[(kSelThreads >> 5) - 1];
+    __syncthreads();
+    return v + add;
+}
+
+__global__ void __launch_bounds__(kSelThreads) k_topk_select(GrState st, int t) {
+    const int r = blockIdx.x;
+    const GrReqDev R = st.req[r];
+    if (t >= R.n_levels) return;
+    const int C = st.C;
+    const int n_live = st.n_beams[r * (st.n_levels + 1) + t];
+    const int N = n_live * C;
+    const uint32_t* keys = st.cand + (int64_t)R.row_off * C;
+    const int k_want = R.width;
+
+    __shared__ int hist[kHistBins];
+    __shared__ int warp_tot[32];
+    __shared__ int sh_digit, sh_kk, sh_count, sh_gt, sh_eqcnt;
+    __shared__ unsigned long long sel[kMaxBeam];
+
+    const int tid = threadIdx.x;
+    // pass 0: count candidates + histogram of bits [31:20]
+    uint32_t prefix = 0, pmask = 0;
+    int kk = k_want;
+    int n_valid = 0;
+    const int shifts[3] = {20, 8, 0};
+    const int widths[3] = {12, 12, 8};
+    bool take_all = false;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int sh = shifts[pass];
+        const uint32_t dmask = (1u << widths[pass]) - 1u;
+        for (int i = tid; i < kHistBins; i += kSelThreads) hist[i] = 0;
+        if (tid == 0) sh_count = 0;
+        __syncthreads();
+        int my_valid = 0;
+        // every lane runs the same trip count so the warp is converged at the match
+        for (int base = 0; base < N; base += kSelThreads) {
+            const int i = base + tid;
+            const uint32_t u = (i < N) ? keys[i] : 0u;
+            const bool q = (u != 0) && ((u & pmask) == prefix);
+            my_valid += (u != 0);
+            const uint32_t bin = q ? ((u >> sh) & dmask) : 0xFFFFFFFFu;
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            if (q && (__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[bin], __popc(peers));
+        }
+        if (pass == 0) {
+            atomicAdd(&sh_count, my_valid);
+            __syncthreads();
+            n_valid = sh_count;
+            if (n_valid <= k_want) { take_all = true; break; }
+        }
+        __syncthreads();
+        // thread j owns bins [nb*(T-1-j), nb*(T-j)) so thread order = descending bin order
+        const int nbins = 1 << widths[pass];
+        const int per = nbins / kSelThreads > 0 ? nbins / kSelThreads : 1;
+        const int owner_active = (tid < nbins / per);
+        int hi = nbins - 1 - tid * per;  // highest bin of this thread
+        int v = 0;
+        if (owner_active)
+            for (int e = 0; e < per; ++e) v += hist[hi - e];
+        int total;
+        const int incl = block_incl_scan(v, warp_tot, total);
+        const int excl = incl - v;
+        if (owner_active && excl < kk && kk <= incl) {
+            int acc = excl;
+            for (int e = 0; e < per; ++e) {
+                const int h = hist[hi - e];
+                if (acc + h >= kk) { sh_digit = hi - e; sh_kk = kk - acc; break; }
+                acc += h;
+            }
+        }
+        __syncthreads();
+        prefix |= (uint32_t)sh_digit << sh;
+        pmask |= dmask << sh;
+        kk = sh_kk;
+        if (pass == 2 && tid == 0) sh_eqcnt = hist[sh_digit];  // keys equal to the threshold
+        __syncthreads();
+    }
+
+    // gather: all keys > tau, plus the first kk keys == tau in flat order
+    const uint32_t tau = take_all ? 0u : prefix;
+    if (tid == 0) sh_gt = 0;
+    __syncthreads();
+    const bool eq_all = take_all || (sh_eqcnt == kk);
+    const int n_take = take_all ? n_valid : k_want;
+    for (int i = tid; i < N; i += kSelThreads) {
+        const uint32_t u = keys[i];
+        const bool pick = take_all ? (u != 0) : (u > tau || (eq_all && u == tau));
+        if (pick) {
+            const int pos = atomicAdd(&sh_gt, 1);
+            sel[pos] = ((unsigned long long)u << 32) | (unsigned)(0xFFFFFFFFu - (uint32_t)i);
+        }
+    }
+    __syncthreads();
+    if (!eq_all) {
+        // ties at the threshold: keep the kk smallest flat indices, in index order
+        int base_rank = 0;
+        for (int start = 0; start < N; start += kSelThreads) {
+            const int i = start + tid;
+            const int e = (i < N && keys[i] == tau) ? 1 : 0;
+            int total;
+            const int incl = block_incl_scan(e, warp_tot, total);
+            const int rank = base_rank + incl - e;
+            if (e && rank < kk) {
+                const int pos = atomicAdd(&sh_gt, 1);
+                sel[pos] = ((unsigned long long)tau << 32) | (unsigned)(0xFFFFFFFFu - (uint32_t)i);
+            }
+            base_rank += total;
+            if (base_rank >= kk) break;
+        }
+        __syncthreads();
+    }
+    // bitonic sort of n_take entries, descending
+    int P = 1;
+    while (P < n_take) P <<= 1;
+    for (int i = n_take + tid; i < P; i += kSelThreads) sel[i] = 0ull;
+    __syncthreads();
+    for (int k = 2; k <= P; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < P; i += kSelThreads) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const unsigned long long a = sel[i], c = sel[ixj];
+                    const bool desc = ((i & k) == 0);
+                    if (desc ? (a < c) : (a > c)) { sel[i] = c; sel[ixj] = a; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = tid; i < n_take; i += kSelThreads) {
+        const unsigned long long e = sel[i];
+        const uint32_t flat = 0xFFFFFFFFu - (uint32_t)(e & 0xFFFFFFFFull);
+        st.sel_parent[R.row_off + i] = (int)(flat / (uint32_t)C);
+        st.sel_code[R.row_off + i] = (int)(flat % (uint32_t)C);
+        st.sel_key[R.row_off + i] = unorder_key((uint32_t)(e >> 32));
+    }
+    if (tid == 0) st.n_sel[r] = n_take;
+}
+
+// ---------------------------------------------------------------------------
+// K5: BeamPath advance (no KV copies)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kMaxBeam) k_advance(GrState st, int t) {
+    const int r = blockIdx.x;
+    const GrReqDev R = st.req[r];
+    if (t >= R.n_levels) return;
+    const int L = st.n_levels;
+    const int n = st.n_sel[r];
+    if (threadIdx.x == 0) st.n_beams[r * (L + 1) + t + 1] = n;
+    const int i = threadIdx.x;
+    if (i >= n) return;
+    const int row = R.row_off + i;
+    const int p = st.sel_parent[row];
+    const int c = st.sel_code[row];
+    const int64_t prow = R.row_off + p;
+    const int64_t pnode = (t == 0) ? 0 : st.node[(int64_t)(t - 1) * st.rows + prow];
+    if (pnode < 0 || pnode >= R.n_nodes) { atomicOr(st.status, kStatusBadNode); return; }
+    const uint32_t* mk = R.mask + pnode * R.mask_words;
+    int rank = 0;
+    for (int w = 0; w < (c >> 5); ++w) rank += __popc(mk[w]);
+    rank += __popc(mk[c >> 5] & ((1u << (c & 31)) - 1u));
+    const int64_t lvl = (int64_t)t * st.rows;
+    st.parent[lvl + row] = p;
+    st.token[lvl + row] = st.code_base + t * st.C + c;
+    st.node[lvl + row] = R.child_base[pnode] + rank;
+    st.score[lvl + row] = st.sel_key[row];
+    int32_t* dst = st.path + (lvl + row) * L;
+    if (t > 0) {
+        const int32_t* src = st.path + ((int64_t)(t - 1) * st.rows + prow) * L;
+        for (int j = 0; j < t; ++j) dst[j] = src[j];
+    }
+    dst[t] = i;
+}
+
+// ---------------------------------------------------------------------------
+// K6: results of the final level
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kMaxBeam) k_results(GrState st) {
+    const int r = blockIdx.x;
+    const GrReqDev R = st.req[r];
+    const int L = R.n_levels;
+    const int n = st.n_beams[r * (st.n_levels + 1) + L];
+    const int i = threadIdx.x;
+    if (i >= n) return;
+    const int row = R.row_off + i;
+    const int64_t last = (int64_t)(L - 1) * st.rows + row;
+    const int32_t* path = st.path + last * st.n_levels;
+    for (int j = 0; j < L; ++j) {
+        const int slot = path[j];
+        const int tok = st.token[(int64_t)j * st.rows + R.row_off + slot];
+        st.res_codes[(int64_t)row * st.n_levels + j] = tok - st.code_base - j * st.C;
+    }
+    const int64_t leaf = (int64_t)st.node[last] - R.leaf_base;
+    st.res_items[row] = (leaf >= 0) ? R.leaf_item[leaf] : -1;
+    st.res_scores[row] = st.score[last];
+}
+
+__global__ void k_init_state(GrState st) {
+    const int L1 = st.n_levels + 1;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < st.n_req * L1; i += gridDim.x * blockDim.x)
+        st.n_beams[i] = (i % L1 == 0) ? 1 : 0;
+    if (blockIdx.x == 0 && threadIdx.x < 4) st.status[threadIdx.x] = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_init_state(const GrState& st, cudaStream_t s) {
+    k_init_state<<<1, 256, 0, s>>>(st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_logsoftmax_gather(const GrState& st, int t, const float* logits, int64_t ld,
+                                     float* logprobs_out, float* lse_out, const float* lse_in,
+                                     cudaStream_t s) {
+    dim3 grid(st.rows * kLogitCluster);
+    k_logsoftmax_gather<<<grid, kLsThreads, 0, s>>>(st, t, logits, ld, logprobs_out, lse_out, lse_in);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk_select(const GrState& st, int t, cudaStream_t s) {
+    k_topk_select<<<st.n_req, kSelThreads, 0, s>>>(st, t);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_advance(const GrState& st, int t, cudaStream_t s) {
+    k_advance<<<st.n_req, kMaxBeam, 0, s>>>(st, t);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_results(const GrState& st, cudaStream_t s) {
+    k_results<<<st.n_req, kMaxBeam, 0, s>>>(st);
+    return cudaGetLastError();
+}
+
+}  // namespace grb

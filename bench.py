@@ -1,0 +1,407 @@
+"""Benchmark of one wide-beam semantic-ID decode step on GB300.
+
+A step is one full-width decode step t = 1 over the whole batch: gr_decode_attn
+for every layer (shared-context tensor-core attention + BeamKV combine), then
+gr_constrained_topk (full-vocabulary log-softmax + item-constrained top-K) and
+gr_beam_advance.  Each timed step first rewinds the handle to step 1 (host
+state only), so every iteration decodes the same full-width step.
+
+Workload (default): 8 requests x context 5000 x beam 256, Qwen3-1.7B attention
+geometry (28 layers, 16 q / 8 KV heads, head_dim 128), vocabulary 151,936,
+3 code levels x 256 codes, 1M uniform items -- the page's long-context shape
+(zhiding.cn recsys-examples article, section "语义ID生成式推荐专用推理框架").
+All tensors are synthetic (seeded normal bf16 Q/K/V, fp32 logits with std 2);
+no model weights.  The ContextKV alone (4.6 GB) is larger than L2, so no
+flush is needed between steps.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle baseline is reported as single-threaded: pin BLAS before numpy loads
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from beam_decode_gb300 import workload as wl  # noqa: E402
+
+METRIC = "GR beam decode-steps/s (ctx 5000, beam 256); attn TC % and HBM GB/s vs peak"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sust": d["bf16_tflops_sustained"],
+                "src": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sust": 1700.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# device batch
+# ---------------------------------------------------------------------------
+class DeviceBatch:
+    """Synthetic batch resident in HBM, decoded through the C ABI."""
+
+    def __init__(self, w: wl.Workload, device="cuda"):
+        import torch
+        from beam_decode_gb300 import binding as B
+        self.w, self.device, self.torch = w, device, torch
+        R = w.n_requests
+        items = wl.workload_items(w)
+        tries = {}
+        self.tries = []
+        for it in items:
+            if id(it) not in tries:
+                tries[id(it)] = B.Trie(it, codes_per_level=w.codes_per_level, device=device)
+            self.tries.append(tries[id(it)])
+        self.items = items
+        self.ctx_off = np.concatenate([[0], np.cumsum(w.ctx_lens)[:-1]]).astype(np.int64)
+        pool = int(sum(w.ctx_lens))
+        shp = (w.n_layers, w.n_kv_heads, pool, w.head_dim)
+        self.ctx_k = torch.empty(shp, dtype=torch.bfloat16, device=device)
+        self.ctx_v = torch.empty(shp, dtype=torch.bfloat16, device=device)
+        for l in range(w.n_layers):  # layer by layer keeps the fp32 temporaries small
+            self.ctx_k[l] = wl.device_normal(shp[1:], w.seed, wl.TAG_CTX_K, device, torch.bfloat16, sub=l)
+            self.ctx_v[l] = wl.device_normal(shp[1:], w.seed, wl.TAG_CTX_V, device, torch.bfloat16, sub=l)
+        reqs = [(int(self.ctx_off[r]), w.ctx_lens[r], w.beam_widths[r], self.tries[r]) for r in range(R)]
+        self.beam = B.Beam(w.n_layers, w.n_q_heads, w.n_kv_heads, w.head_dim, w.vocab, w.code_base, w.n_levels,
+                           w.codes_per_level, self.ctx_k, self.ctx_v, reqs, device=device)
+        rows = self.beam.rows
+        self.rows = rows
+        qs = (rows, w.n_q_heads, w.head_dim)
+        self.q = [wl.device_normal(qs, w.seed, wl.TAG_Q, device, torch.bfloat16, sub=l) for l in range(w.n_layers)]
+        self.out = [torch.empty(qs, dtype=torch.bfloat16, device=device) for _ in range(w.n_layers)]
+        self.logits = [wl.device_normal((rows, w.vocab), w.seed, wl.TAG_LOGITS, device, std=w.logit_std, sub=t)
+                       for t in range(2)]
+        kvs = (rows, w.n_kv_heads, w.head_dim)
+        self.new_k = [wl.device_normal(kvs, w.seed, wl.TAG_BEAM_K, device, torch.bfloat16, sub=l)
+                      for l in range(w.n_layers)]
+        self.new_v = [wl.device_normal(kvs, w.seed, wl.TAG_BEAM_V, device, torch.bfloat16, sub=l)
+                      for l in range(w.n_layers)]
+        # step 0: level-0 codes from the prefill logits, then feed level-0 K/V
+        self.beam.constrained_topk(self.logits[0])
+        self.beam.advance()
+        for l in range(w.n_layers):
+            k, v = self.beam.kv_slot(l)
+            k.copy_(self.new_k[l])
+            v.copy_(self.new_v[l])
+        torch.cuda.synchronize()
+
+    def step(self):
+        """One full-width decode step t = 1 (device-resident inputs)."""
+        b = self.beam
+        b.rewind(1)
+        for l in range(self.w.n_layers):
+            b.decode_attn(l, self.q[l], self.out[l])
+        b.constrained_topk(self.logits[1])
+        b.advance()
+
+    # algorithmic work of one step
+    def attn_flops(self) -> float:
+        w = self.w
+        return float(sum(4.0 * w.n_layers * w.n_q_heads * W * T * w.head_dim
+                         for W, T in zip(w.beam_widths, w.ctx_lens)))
+
+    def ctx_bytes_per_layer(self) -> float:
+        w = self.w
+        return float(sum(T for T in w.ctx_lens) * w.n_kv_heads * w.head_dim * 2 * 2)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampling
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_step_seconds(w: wl.Workload, budget_s: float = 12.0):
+    """Seconds per decode step of the CPU oracle, from a bounded sample:
+    naive per-beam attention for a sample of (beam, layer) pairs of request 0
+    and the constrained top-K of request 0 (full rows), scaled to the step."""
+    from oracle import OracleBeam, Trie, beam_attention
+    rng_seed = w.seed
+    T, W, D = w.ctx_lens[0], w.beam_widths[0], w.head_dim
+    ck = wl.round_to_bf16(wl.host_normal((w.n_kv_heads, T, D), rng_seed, wl.TAG_CTX_K)).astype(np.float64)
+    cv = wl.round_to_bf16(wl.host_normal((w.n_kv_heads, T, D), rng_seed, wl.TAG_CTX_V)).astype(np.float64)
+    q = wl.round_to_bf16(wl.host_normal((W, w.n_q_heads, D), rng_seed, wl.TAG_Q)).astype(np.float64)
+    bk = [wl.round_to_bf16(wl.host_normal((W, w.n_kv_heads, D), rng_seed, wl.TAG_BEAM_K)).astype(np.float64)]
+    bv = [wl.round_to_bf16(wl.host_normal((W, w.n_kv_heads, D), rng_seed, wl.TAG_BEAM_V)).astype(np.float64)]
+    anc = [[b] for b in range(W)]
+    t0 = time.perf_counter()
+    n_att = 0
+    while time.perf_counter() - t0 < budget_s * 0.5 and n_att < W:
+        beam_attention(q, ck, cv, bk, bv, anc, beams=[n_att])
+        n_att += 1
+    att_s = (time.perf_counter() - t0) / n_att  # one (beam, layer): all q heads
+    # top-K of one request at step 1 (full width)
+    items = wl.draw_items(min(w.n_items[0], 200_000), w.n_levels, w.codes_per_level, w.trie_dist, w.seed)
+    trie = Trie(items, codes_per_level=w.codes_per_level)
+    ob = OracleBeam(trie, W, w.n_levels, w.codes_per_level, w.code_base)
+    x0 = wl.host_normal((1, w.vocab), rng_seed, wl.TAG_LOGITS, std=w.logit_std)
+    ob.step(x0)
+    n1 = ob.n_live()
+    x1 = wl.host_normal((n1, w.vocab), rng_seed, wl.TAG_LOGITS, sub=(1,), std=w.logit_std)
+    t1 = time.perf_counter()
+    ob.step(x1)
+    topk_s = (time.perf_counter() - t1) * (W / max(n1, 1))
+    per_step = (att_s * W * w.n_layers + topk_s) * w.n_requests
+    sample = (f"oracle on request 0: naive float64 attention of {n_att} beams x {w.n_q_heads} heads at one layer "
+              f"({att_s * 1e3:.1f} ms per beam-layer) scaled x{W} beams x{w.n_layers} layers x{w.n_requests} "
+              f"requests; constrained top-K of {n1} live rows ({topk_s:.2f} s) x{w.n_requests} requests")
+    return per_step, sample
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    times = []
+    sample = ""
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state
+    for _ in range(max(args.steps, 1)):
+        s, sample = oracle_step_seconds(w, budget_s=min(20.0, 60.0 / max(args.steps, 1)))
+        times.append(s)
+    sec = float(np.mean(times))
+    value = 1.0 / sec
+    line = {"metric": METRIC, "value": value, "unit": "steps/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "requests": w.n_requests, "ctx": w.ctx_lens[0], "beam": w.beam_widths[0],
+                       "levels": w.n_levels, "codes": w.codes_per_level, "vocab": w.vocab},
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args, w):
+    import torch
+    import torch.distributed as dist
+    from beam_decode_gb300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = f"cuda:{local}"
+    # replicas only: each rank decodes its own batch (seed offset by rank)
+    if rank:
+        w = wl.make_workload(w.name, seed=w.seed + 1000 * rank)
+    batch = DeviceBatch(w, dev)
+    beam = batch.beam
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        batch.step()
+    torch.cuda.synchronize()
+    if beam.status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    for k in range(B.KERNEL_KINDS):
+        beam.kernel_stats(k, reset=True)
+    beam.set_timing(True)
+    clocks = Clocks(local)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        batch.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    ck = clocks.stop()
+    beam.set_timing(False)
+    stats = {B.KERNEL_NAMES[k]: beam.kernel_stats(k, reset=True) for k in range(B.KERNEL_KINDS)}
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * 1000.0 / ms_per_step
+    launches = sum(n for (n, _) in stats.values())
+    st = beam.status()
+    if st != 0:
+        raise RuntimeError(f"device status error {st}")
+
+    # roofline of the dominant kernel (shared-context attention)
+    pk = _peaks()
+    n_att, t_att = stats["ctx_attn"]
+    att_ms = t_att / max(n_att, 1)
+    flops_launch = batch.attn_flops() / w.n_layers
+    achieved = flops_launch / (att_ms * 1e-3) / 1e12
+    peak = pk["bf16_sust"]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "kernel": "k_ctx_attn",
+                "peak_kind": f"{pk['src']} sustained bf16"}
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, batch) if rank == 0 else None
+
+    per_kernel = {k: {"launches": n, "ms_per_launch": (t / n if n else 0.0), "ms_per_step": t / args.steps}
+                  for k, (n, t) in stats.items() if n}
+    hbm = {}
+    for name in ("beam_attn", "logsoftmax_gather"):
+        n, t = stats[name]
+        if n:
+            if name == "logsoftmax_gather":
+                byts = batch.rows * w.vocab * 4.0
+            else:
+                byts = batch.rows * w.n_q_heads * w.head_dim * 2 * 2 + batch.rows * w.n_kv_heads * w.head_dim * 2 * 2
+            hbm[name] = {"GB_s": byts / (t / n * 1e-3) / 1e9, "frac": byts / (t / n * 1e-3) / 1e9 / pk["hbm"]}
+
+    if rank == 0:
+        cpu_s, sample = oracle_step_seconds(w, budget_s=12.0) if not args.no_cpu else (float("nan"), "skipped")
+        line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "requests": w.n_requests, "ctx": w.ctx_lens[0],
+                           "beam": w.beam_widths[0], "layers": w.n_layers, "q_heads": w.n_q_heads,
+                           "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "vocab": w.vocab,
+                           "levels": w.n_levels, "codes": w.codes_per_level, "items": w.n_items[0],
+                           "l2": "inputs larger than L2 (ContextKV 4.6 GB)", "parallelism": f"replicas{world}"},
+                "roofline": roofline,
+                "hbm_kernels": hbm,
+                "kernels": per_kernel,
+                "cpu_baseline": {"value": 1.0 / cpu_s if cpu_s == cpu_s else None, "unit": "steps/s", "cores": 1,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": e2e,
+                "gpu_launches": launches,
+                "clocks": ck}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, batch: DeviceBatch):
+    """Same step through the public API with pinned host inputs copied in and
+    the step's selection read back every step."""
+    import torch
+    w = batch.w
+    beam = batch.beam
+    host_q = [q.cpu().pin_memory() for q in batch.q]
+    host_k = [k.cpu().pin_memory() for k in batch.new_k]
+    host_v = [v.cpu().pin_memory() for v in batch.new_v]
+    host_x = batch.logits[1].cpu().pin_memory()
+    dq = [torch.empty_like(q) for q in batch.q]
+    dx = torch.empty_like(batch.logits[1])
+    h2d = sum(t.numel() * t.element_size() for t in host_q + host_k + host_v) + host_x.numel() * 4
+    d2h = 0
+
+    def one():
+        nonlocal d2h
+        beam.rewind(1)
+        for l in range(w.n_layers):
+            k, v = beam.kv_slot(l)
+            k.copy_(host_k[l], non_blocking=True)
+            v.copy_(host_v[l], non_blocking=True)
+            dq[l].copy_(host_q[l], non_blocking=True)
+            beam.decode_attn(l, dq[l], batch.out[l])
+        dx.copy_(host_x, non_blocking=True)
+        beam.constrained_topk(dx)
+        beam.advance()
+        n = 0
+        for r in range(w.n_requests):
+            par, tok, nod, sc = beam.path(r, 1)
+            n += (par.nbytes + tok.nbytes + sc.nbytes)
+        d2h = n
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 4)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": 1.0 / dt, "unit": "steps/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gr", choices=["gr", "reference"])
+    ap.add_argument("--workload", default="long", choices=["tiny", "page1", "short", "long", "mixed"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    w = wl.make_workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    from beam_decode_gb300.build import build
+    build()
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,257 @@
+/*
+ * grbeam.h -- C ABI of the GB300 wide-beam semantic-ID decode step.
+ *
+ * One decode step of semantic-ID generative recommendation with a split KV
+ * layout, as described in the zhiding.cn article on NVIDIA recsys-examples,
+ * section "语义ID生成式推荐专用推理框架" (semantic-ID GR inference framework):
+ *   - ContextKV: the long request context, stored once per request and shared
+ *     by all of its beams;
+ *   - BeamKV:    the short history of tokens each beam decoded itself;
+ *   - BeamPath:  the beams' ancestry, so no beam is stored as an independent
+ *                long sequence;
+ *   - dynamic beam width and item-constrained top-K.
+ * Beam search returns every surviving beam, not only the best ("Advancing
+ * Generative Recommendation Inference: our collaboration with NVIDIA on
+ * TensorRT LLM", section "Background: what inference a recommendation request
+ * needs").
+ *
+ * One step t (t = 0 .. L-1, L = semantic-ID length) is, in call order:
+ *   [t >= 1] for every layer: the caller writes the K/V of the token chosen at
+ *            level t-1 into gr_beam_kv_slot(), then calls gr_decode_attn();
+ *   gr_constrained_topk() on the step's logit rows (for t = 0: the prefill
+ *            logits, one live row per request);
+ *   gr_beam_advance().
+ * After step L-1, gr_beam_results() returns all beams of a request.
+ *
+ * Conventions
+ *   - Memory: the caller allocates and owns every device buffer (ContextKV
+ *     pool, BeamKV pool, workspace, trie buffer, inputs, outputs).  The library
+ *     never allocates device memory; a handle owns host metadata only.
+ *   - Streams: gr_stream_t is a cudaStream_t (NULL = legacy default stream).
+ *     Every call that takes a stream only enqueues work on it, except
+ *     gr_beam_results / gr_beam_path / gr_beam_status, which synchronise it.
+ *   - Rows: request r owns the contiguous rows [row_off[r], row_off[r] + W_r)
+ *     of every per-row tensor (queries, attention output, logits, BeamKV
+ *     slots); W_r is the request's maximum beam width.  Row b of request r is
+ *     beam slot b.  Rows of beams that are not live at this step are ignored
+ *     on input and written as zeros (attention) or left untouched (top-K).
+ *   - Errors: argument, state and capacity errors are returned synchronously
+ *     and leave the handle unchanged.  Errors that only the device can see
+ *     (a NaN key, a timed-out wait) set a status word that gr_beam_status(),
+ *     gr_beam_results() and gr_beam_path() report as GR_ERR_DEVICE /
+ *     GR_ERR_TIMEOUT.  gr_last_error() gives a message for the calling thread.
+ *     No C++ exception crosses this interface.
+ *   - Threads: a handle may be used by one thread at a time.
+ */
+#ifndef GRBEAM_H_
+#define GRBEAM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int gr_status;
+#define GR_OK               0
+#define GR_ERR_INVALID_ARG (-1)  /* bad pointer, size, alignment or value      */
+#define GR_ERR_UNSUPPORTED (-2)  /* valid but not supported by this build      */
+#define GR_ERR_CAPACITY    (-3)  /* buffer too small / size above a maximum    */
+#define GR_ERR_STATE       (-4)  /* call out of order for the current step     */
+#define GR_ERR_CUDA        (-5)  /* a CUDA runtime call failed                 */
+#define GR_ERR_TIMEOUT     (-6)  /* a device-side wait gave up                 */
+#define GR_ERR_DEVICE      (-7)  /* a kernel flagged invalid data (NaN key...) */
+
+typedef void* gr_stream_t;          /* cudaStream_t */
+typedef struct gr_trie gr_trie;     /* item catalogue on the device */
+typedef struct gr_beam gr_beam;     /* one batch of requests being decoded */
+
+/* Model geometry and code layout of a batch. */
+typedef struct {
+    int n_layers;          /* attention layers                                  */
+    int n_q_heads;         /* Hq                                                */
+    int n_kv_heads;        /* Hkv; Hq % Hkv == 0; query head q reads KV head q / (Hq/Hkv) */
+    int head_dim;          /* D: 64 or 128                                      */
+    int vocab;             /* V: length of a logit row                          */
+    int code_base;         /* token id of (level 0, code 0)                     */
+    int n_levels;          /* L: codes per item (1..8)                          */
+    int codes_per_level;   /* C: codes per level (1..1024)                      */
+    int64_t pool_tokens;   /* tokens per (layer, KV head) in the ContextKV pool */
+} gr_config;
+/* Level-t code c is vocabulary token code_base + t*C + c; the L*C code tokens
+ * must lie inside [0, vocab). */
+
+/* One request of the batch. */
+typedef struct {
+    int64_t ctx_offset;    /* first token of this request in the ContextKV pool */
+    int ctx_len;           /* T_r >= 1; ctx_offset + T_r <= pool_tokens         */
+    int beam_width;        /* W_r: maximum beams, 1..1024                       */
+    const gr_trie* trie;   /* catalogue; its n_levels / C must match gr_config  */
+} gr_request;
+
+/* Device buffers of a batch (all owned by the caller). */
+typedef struct {
+    const void* ctx_k;     /* bf16 [n_layers][n_kv_heads][pool_tokens][head_dim] */
+    const void* ctx_v;     /* same layout as ctx_k                               */
+    void* beam_k;          /* bf16 [n_layers][n_levels-1][rows][n_kv_heads][head_dim],
+                              gr_beam_kv_bytes() bytes; NULL allowed when n_levels == 1 */
+    void* beam_v;          /* same layout as beam_k                              */
+    void* workspace;       /* gr_beam_workspace_bytes() bytes, 256-byte aligned  */
+    size_t workspace_bytes;
+} gr_buffers;
+
+/* ------------------------------------------------------------------------ */
+/* Item catalogue (item-constrained generation)                             */
+/* ------------------------------------------------------------------------ */
+
+/* Device bytes needed by gr_trie_create for these items.
+ * codes: host int32 [n_items][n_levels], each in [0, codes_per_level). */
+gr_status gr_trie_device_bytes(const int32_t* codes, int64_t n_items, int n_levels,
+                               int codes_per_level, size_t* bytes);
+
+/* Build the prefix trie of the items on the host and upload it into dev_buf
+ * (caller-owned device memory of at least gr_trie_device_bytes(), 256-byte
+ * aligned) with one asynchronous copy on `stream`; the host staging copy is
+ * released once the copy completes (the call waits for it).
+ * item_ids: host int64 [n_items] returned by gr_beam_results, or NULL for
+ * 0..n_items-1.  Duplicate code tuples -> GR_ERR_INVALID_ARG.
+ * Each inner node stores a bitmask of its valid child codes and the index of
+ * its first child; a child is found by the rank of its code in the mask. */
+gr_status gr_trie_create(const int32_t* codes, const int64_t* item_ids, int64_t n_items,
+                         int n_levels, int codes_per_level, void* dev_buf, size_t dev_bytes,
+                         gr_stream_t stream, gr_trie** out);
+gr_status gr_trie_destroy(gr_trie* trie);   /* host object only; dev_buf stays the caller's */
+
+/* ------------------------------------------------------------------------ */
+/* Batch handle                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes for this batch (schedule, attention partials, candidate
+ * keys, selection, BeamPath, results staging, status word). */
+gr_status gr_beam_workspace_bytes(const gr_config* cfg, const gr_request* reqs, int n_requests,
+                                  size_t* bytes);
+/* Bytes of ONE BeamKV tensor (K or V) for this batch. */
+gr_status gr_beam_kv_bytes(const gr_config* cfg, const gr_request* reqs, int n_requests,
+                           size_t* bytes);
+
+/* Validate the batch, carve the workspace, upload the request table, the
+ * attention schedule and the TMA descriptors of the ContextKV pool, and put
+ * every request at step 0 with one root beam of score 0 (enqueued on
+ * `stream`).  The handle stays valid until gr_beam_destroy. */
+gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs, int n_requests,
+                         const gr_buffers* bufs, gr_stream_t stream, gr_beam** out);
+gr_status gr_beam_destroy(gr_beam* beam);
+
+/* rows_total = sum of W_r; row_offsets (optional, n_requests+1 ints) gets the
+ * first row of each request and rows_total last. */
+gr_status gr_beam_rows(const gr_beam* beam, int* rows_total, int* row_offsets);
+/* Current step t (0..L; L means decoding is finished). */
+gr_status gr_beam_step(const gr_beam* beam, int* step);
+
+/* Zero-copy view of BeamKV for the token chosen at level t-1 (t = current
+ * step >= 1): bf16 [rows][n_kv_heads][head_dim] for `layer`.  The caller writes
+ * each live beam's new K and V there (slot b = row b) before gr_decode_attn. */
+gr_status gr_beam_kv_slot(gr_beam* beam, int layer, void** k_new, void** v_new);
+
+/* ------------------------------------------------------------------------ */
+/* Hot path                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* GQA decode attention of every live beam at the current step t >= 1, layer
+ * `layer`: beam b of request r attends to its request's T_r context tokens
+ * followed by the t BeamKV tokens on its path (levels 0..t-1, slots from
+ * BeamPath), scale 1/sqrt(D).
+ *   q   bf16 [rows][n_q_heads][head_dim], 16-byte aligned
+ *   out bf16 [rows][n_q_heads][head_dim]; dead rows are written as zeros
+ * The context part runs on the tensor cores (tcgen05, TMA-fed, every context
+ * byte read once per request), the BeamKV part with vector loads, merged by
+ * a log-sum-exp combine.  Each layer may be called once per step. */
+gr_status gr_decode_attn(gr_beam* beam, int layer, const void* q, void* out, gr_stream_t stream);
+
+/* Full-vocabulary log-softmax of every live row, then the item-constrained
+ * top-K of each request across (beam, code) candidates of level t:
+ *   key(b, c) = S_b + (x[b][code_base + t*C + c] - LSE_b)   (float32, each
+ *   operation rounded once), over codes c valid after beam b's prefix;
+ *   order: key descending, then flat index b*C + c ascending;
+ *   the first min(W_r, #candidates) survive (dynamic width).
+ *   logits        fp32 [rows][ld], ld >= vocab, ld % 4 == 0, 16-byte aligned;
+ *                 for t = 0 only row row_off[r] of each request is read
+ *   logprobs_out  optional fp32 [rows][C]: x - LSE of the level's codes,
+ *                 -inf for invalid codes (live rows only)
+ *   lse_out       optional fp32 [rows]: LSE_b (live rows only)
+ *   lse_in        optional fp32 [rows]: use these LSE_b instead of computing
+ *                 them (for bit-exact comparison with a reference)
+ * The selection is kept in the workspace until gr_beam_advance. */
+gr_status gr_constrained_topk(gr_beam* beam, const float* logits, int64_t ld, float* logprobs_out,
+                              float* lse_out, const float* lse_in, gr_stream_t stream);
+
+/* Commit the selection of step t to BeamPath (parent slot, token, trie node,
+ * score, ancestry) and set the live width of step t+1; no KV is moved.  The
+ * step counter becomes t+1. */
+gr_status gr_beam_advance(gr_beam* beam, gr_stream_t stream);
+
+/* Set the step counter back to `step` (1 <= step <= current step) so that
+ * step `step` can be decoded again from the BeamPath levels before it (host
+ * state only; nothing is enqueued). */
+gr_status gr_beam_rewind(gr_beam* beam, int step);
+
+/* All surviving beams of request `request` after the last step, best first
+ * (synchronises `stream`):
+ *   codes     int32 [W_r][n_levels]   code of each level
+ *   item_ids  int64 [W_r]             item of the code string
+ *   scores    fp32  [W_r]             sum of the code log-probabilities
+ *   n_out     number of beams written
+ * Reports a device status error if a kernel flagged one. */
+gr_status gr_beam_results(gr_beam* beam, int request, int32_t* codes, int64_t* item_ids,
+                          float* scores, int* n_out, gr_stream_t stream);
+
+/* BeamPath of one level (synchronises `stream`): for the n_out beams that
+ * level t produced, parent slot at level t-1, token id, trie node id, score.
+ * Any output pointer may be NULL. */
+gr_status gr_beam_path(gr_beam* beam, int request, int level, int32_t* parents, int32_t* tokens,
+                       int32_t* nodes, float* scores, int* n_out, gr_stream_t stream);
+
+/* Synchronise `stream` and report the device status word (GR_OK,
+ * GR_ERR_DEVICE or GR_ERR_TIMEOUT); clear_flag != 0 clears it afterwards. */
+gr_status gr_beam_status(gr_beam* beam, int clear_flag, gr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Measurement                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Kernel kinds, for gr_beam_kernel_stats. */
+#define GR_KERNEL_CTX_ATTN    0  /* shared-context attention (tensor cores)        */
+#define GR_KERNEL_BEAM_ATTN   1  /* BeamKV attention + log-sum-exp combine          */
+#define GR_KERNEL_LOGSOFTMAX  2  /* full-vocab log-softmax + level gather + mask    */
+#define GR_KERNEL_TOPK        3  /* cross-beam top-K selection per request          */
+#define GR_KERNEL_ADVANCE     4  /* BeamPath advance                                */
+#define GR_KERNEL_RESULTS     5  /* result gather                                    */
+#define GR_KERNEL_INIT        6  /* state initialisation                             */
+#define GR_KERNEL_KINDS       7
+
+/* enable != 0: bracket every kernel launch with CUDA events on its stream
+ * (host-side event objects; no device memory). */
+gr_status gr_beam_set_timing(gr_beam* beam, int enable);
+/* Launch count of a kernel kind since the last reset and, if timing was on,
+ * the summed device time in milliseconds (synchronises the timed events).
+ * reset != 0 clears the counters after reading. */
+gr_status gr_beam_kernel_stats(gr_beam* beam, int kind, int64_t* launches, double* total_ms, int reset);
+
+/* Test hook: limit (in nanoseconds) of every pipeline wait inside the
+ * attention kernel (a thread waiting for data, for a tensor-core result or
+ * for another warp); 0 restores the default of 2 s.  A wait that exceeds it
+ * makes the kernel stop: it sets GR_ERR_TIMEOUT in the status word, drains
+ * the copies and tensor-core operations it already issued (with a fixed
+ * limit that this hook does not change), frees its tensor memory and
+ * returns; the CUDA context stays usable.  A negative value makes every
+ * pipeline wait give up on its first check, for fault-path tests. */
+gr_status gr_beam_set_wait_limit(gr_beam* beam, int64_t nanoseconds);
+
+const char* gr_status_str(gr_status status);
+const char* gr_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GRBEAM_H_ */

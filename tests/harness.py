@@ -1,0 +1,230 @@
+"""Lock-step harness: the CUDA path (through the C ABI) and the CPU oracle are
+fed the same seeded inputs, step by step, and their outputs compared.
+
+Inputs come only from ``beam_decode_gb300.workload``; expected values come
+only from ``oracle``.  Nothing computed by the CUDA path is fed to the oracle:
+the oracle keeps its own beams, ancestry and BeamKV copy.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional
+
+import numpy as np
+
+from beam_decode_gb300 import workload as wl
+from oracle import OracleBeam, Trie as OTrie, beam_attention
+
+ATOL = 1e-2   # attention: |gpu - ref| <= ATOL + RTOL*|ref| (bf16 K/V, fp32 accumulate)
+RTOL = 1e-2
+LP_TOL = 1e-4  # log-probabilities and log-sum-exp
+
+
+@dataclasses.dataclass
+class Spec:
+    n_layers: int = 1
+    n_q_heads: int = 2
+    n_kv_heads: int = 1
+    head_dim: int = 64
+    vocab: int = 1024
+    n_levels: int = 2
+    codes_per_level: int = 16
+    code_base: int = 512
+    ctx_lens: List[int] = dataclasses.field(default_factory=lambda: [64])
+    widths: List[int] = dataclasses.field(default_factory=lambda: [4])
+    n_items: List[int] = dataclasses.field(default_factory=lambda: [50])
+    trie_dist: str = "uniform"
+    shared_trie: bool = True
+    logit_std: float = 2.0
+    ld_pad: int = 0
+    seed: int = 0
+    pool_gap: int = 7      # unused tokens between requests in the ContextKV pool
+
+    @staticmethod
+    def from_workload(w: wl.Workload, **over) -> "Spec":
+        s = Spec(n_layers=w.n_layers, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
+                 vocab=w.vocab, n_levels=w.n_levels, codes_per_level=w.codes_per_level, code_base=w.code_base,
+                 ctx_lens=list(w.ctx_lens), widths=list(w.beam_widths), n_items=list(w.n_items),
+                 trie_dist=w.trie_dist, shared_trie=w.shared_trie, logit_std=w.logit_std, seed=w.seed)
+        for k, v in over.items():
+            setattr(s, k, v)
+        return s
+
+
+def make_items(spec: Spec) -> List[np.ndarray]:
+    if spec.shared_trie:
+        it = wl.draw_items(spec.n_items[0], spec.n_levels, spec.codes_per_level, spec.trie_dist, spec.seed)
+        return [it] * len(spec.ctx_lens)
+    return [wl.draw_items(n, spec.n_levels, spec.codes_per_level, spec.trie_dist, spec.seed, stream=(r,))
+            for r, n in enumerate(spec.n_items)]
+
+
+class LockStep:
+    """GPU batch + oracle beams over the same host-generated inputs."""
+
+    def __init__(self, spec: Spec, device="cuda", key_mode="f32", logits_fn=None):
+        import torch
+        from beam_decode_gb300 import binding as B
+        self.spec, self.device, self.torch, self.B = spec, device, torch, B
+        self.logits_fn = logits_fn
+        s = spec
+        R = len(s.ctx_lens)
+        self.items = make_items(s)
+        # catalogues (GPU tries share the array when the catalogue is shared)
+        cache: Dict[int, tuple] = {}
+        self.gtries, self.otries = [], []
+        for it in self.items:
+            key = id(it)
+            if key not in cache:
+                cache[key] = (B.Trie(it, codes_per_level=s.codes_per_level, device=device),
+                              OTrie(it, codes_per_level=s.codes_per_level))
+            self.gtries.append(cache[key][0])
+            self.otries.append(cache[key][1])
+        # ContextKV pool with gaps between requests
+        self.ctx_off = []
+        off = 3
+        for T in s.ctx_lens:
+            self.ctx_off.append(off)
+            off += T + s.pool_gap
+        pool = off
+        shp = (s.n_layers, s.n_kv_heads, pool, s.head_dim)
+        self.ctx_k = wl.round_to_bf16(wl.host_normal(shp, s.seed, wl.TAG_CTX_K))
+        self.ctx_v = wl.round_to_bf16(wl.host_normal(shp, s.seed, wl.TAG_CTX_V))
+        tk = torch.from_numpy(self.ctx_k).to(torch.bfloat16).to(device)
+        tv = torch.from_numpy(self.ctx_v).to(torch.bfloat16).to(device)
+        reqs = [(self.ctx_off[r], s.ctx_lens[r], s.widths[r], self.gtries[r]) for r in range(R)]
+        self.beam = B.Beam(s.n_layers, s.n_q_heads, s.n_kv_heads, s.head_dim, s.vocab, s.code_base, s.n_levels,
+                           s.codes_per_level, tk, tv, reqs, device=device)
+        self.row_off = self.beam.row_offsets
+        self.obeams = [OracleBeam(self.otries[r], s.widths[r], s.n_levels, s.codes_per_level, s.code_base,
+                                  key_mode=key_mode) for r in range(R)]
+        # oracle copy of BeamKV: [layer][level] -> [rows, Hkv, D]
+        self.obk = [[None] * max(s.n_levels - 1, 1) for _ in range(s.n_layers)]
+        self.obv = [[None] * max(s.n_levels - 1, 1) for _ in range(s.n_layers)]
+        self.t = 0
+
+    # -- inputs -----------------------------------------------------------------
+    def logits(self, t: int) -> np.ndarray:
+        s = self.spec
+        ld = s.vocab + s.ld_pad
+        x = wl.host_normal((self.beam.rows, ld), s.seed, wl.TAG_LOGITS, sub=(t,), std=s.logit_std)
+        if self.logits_fn is not None:
+            x = np.ascontiguousarray(self.logits_fn(self, t, x), dtype=np.float32)
+        return x
+
+    def write_beam_kv(self, t: int, layer: int):
+        s = self.spec
+        shp = (self.beam.rows, s.n_kv_heads, s.head_dim)
+        k = wl.round_to_bf16(wl.host_normal(shp, s.seed, wl.TAG_BEAM_K, sub=(t, layer)))
+        v = wl.round_to_bf16(wl.host_normal(shp, s.seed, wl.TAG_BEAM_V, sub=(t, layer)))
+        gk, gv = self.beam.kv_slot(layer)
+        gk.copy_(self.torch.from_numpy(k).to(self.torch.bfloat16))
+        gv.copy_(self.torch.from_numpy(v).to(self.torch.bfloat16))
+        self.obk[layer][t - 1], self.obv[layer][t - 1] = k, v
+
+    def queries(self, t: int, layer: int) -> np.ndarray:
+        s = self.spec
+        return wl.round_to_bf16(wl.host_normal((self.beam.rows, s.n_q_heads, s.head_dim), s.seed, wl.TAG_Q,
+                                               sub=(t, layer)))
+
+    # -- one attention layer -------------------------------------------------------
+    def attention(self, layer: int, requests=None, beams_per_request=None) -> Dict:
+        """Run gr_decode_attn for `layer` at the current step; compare with the oracle.
+        Returns the max violation ratio (<= 1 passes) and sizes compared."""
+        torch = self.torch
+        s, t = self.spec, self.t
+        self.write_beam_kv(t, layer)
+        q = self.queries(t, layer)
+        gq = torch.from_numpy(q).to(torch.bfloat16).to(self.device)
+        gout = torch.full_like(gq, float("nan"))
+        self.beam.decode_attn(layer, gq, gout)
+        out = gout.float().cpu().numpy()
+        worst, n = 0.0, 0
+        reqs = range(len(s.ctx_lens)) if requests is None else requests
+        for r in reqs:
+            ob = self.obeams[r]
+            n_live = ob.n_live()
+            r0, T, o0 = self.row_off[r], s.ctx_lens[r], self.ctx_off[r]
+            beams = list(range(n_live)) if beams_per_request is None else \
+                [b for b in beams_per_request if b < n_live]
+            anc = ob.ancestry()
+            ck = self.ctx_k[layer, :, o0:o0 + T]
+            cv = self.ctx_v[layer, :, o0:o0 + T]
+            bk = [self.obk[layer][j][r0:r0 + s.widths[r]] for j in range(t)]
+            bv = [self.obv[layer][j][r0:r0 + s.widths[r]] for j in range(t)]
+            ref = beam_attention(q[r0:r0 + s.widths[r]], ck, cv, bk, bv, anc, beams=beams)
+            got = out[r0 + np.array(beams)]
+            viol = np.abs(got - ref) / (ATOL + RTOL * np.abs(ref))
+            worst = max(worst, float(np.nanmax(viol)) if viol.size else 0.0)
+            if np.isnan(got).any():
+                worst = float("inf")
+            n += viol.size
+            # rows of dead beams are written as zeros
+            dead = out[r0 + n_live:r0 + s.widths[r]]
+            if dead.size and not np.all(dead == 0):
+                worst = float("inf")
+        return {"worst": worst, "n": n}
+
+    # -- one top-K step ----------------------------------------------------------------
+    def topk_step(self, lse_mode: bool = True) -> Dict:
+        """gr_constrained_topk + gr_beam_advance vs the oracle step.
+        lse_mode: pass the oracle's float32 LSE to the GPU (bit-exact contract)."""
+        torch = self.torch
+        s, t = self.spec, self.t
+        x = self.logits(t)
+        R = len(s.ctx_lens)
+        ld = x.shape[1]
+        gx = torch.from_numpy(x).to(self.device)
+        lp_out = torch.full((self.beam.rows, s.codes_per_level), float("nan"), device=self.device)
+        lse_out = torch.full((self.beam.rows,), float("nan"), device=self.device)
+        lse_in = None
+        oinfo = []
+        # oracle first (needs only host data); its float32 LSE is the GPU's lse_in
+        lse32 = np.full(self.beam.rows, np.nan, dtype=np.float32)
+        for r in range(R):
+            ob = self.obeams[r]
+            n = ob.n_live()
+            r0 = self.row_off[r]
+            rows = x[r0:r0 + n, :s.vocab]
+            from oracle import log_softmax_row
+            lses = [log_softmax_row(rw)[1] for rw in rows]
+            lse32[r0:r0 + n] = np.array(lses, dtype=np.float32)
+            info = ob.step(rows, lse_in=lse32[r0:r0 + n] if lse_mode else None)
+            info["lse64"] = lses
+            oinfo.append(info)
+        if lse_mode:
+            lse_in = torch.from_numpy(np.nan_to_num(lse32, nan=0.0)).to(self.device)
+        self.beam.constrained_topk(gx, ld=ld, logprobs_out=lp_out, lse_out=lse_out, lse_in=lse_in)
+        self.beam.advance()
+        res = {"lse_err": 0.0, "lp_err": 0.0, "mismatch": [], "n_sel": []}
+        lse_g = lse_out.cpu().numpy()
+        lp_g = lp_out.cpu().numpy()
+        for r in range(R):
+            info = oinfo[r]
+            r0 = self.row_off[r]
+            n = len(info["lse64"])
+            if not lse_mode:
+                res["lse_err"] = max(res["lse_err"], float(np.max(np.abs(lse_g[r0:r0 + n] - np.array(info["lse64"])))))
+                ref_lp = info["logprobs"]
+                fin = np.isfinite(ref_lp)
+                got = lp_g[r0:r0 + n]
+                if not np.array_equal(np.isfinite(got), fin):
+                    res["lp_err"] = float("inf")
+                else:
+                    res["lp_err"] = max(res["lp_err"], float(np.max(np.abs(got[fin] - ref_lp[fin]), initial=0.0)))
+            par, tok, nod, sc = self.beam.path(r, t)
+            ob = self.obeams[r]
+            exp_par = np.array(ob.parents[t], dtype=np.int32)
+            exp_tok = np.array([s.code_base + t * s.codes_per_level + c for c in ob.codes[t]], dtype=np.int32)
+            exp_sc = np.array([float(v) for v in ob.scores[t]], dtype=np.float32)
+            res["n_sel"].append(len(par))
+            ok = (len(par) == len(exp_par) and np.array_equal(par, exp_par) and np.array_equal(tok, exp_tok))
+            if lse_mode:
+                ok = ok and np.array_equal(sc.view(np.uint32), exp_sc.view(np.uint32))
+            if not ok:
+                res["mismatch"].append(r)
+        self.t += 1
+        return res
+
+    def gpu_results(self, r: int):
+        return self.beam.results(r)

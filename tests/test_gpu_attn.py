@@ -1,0 +1,65 @@
+"""gr_decode_attn against the oracle's naive per-beam attention.
+
+Shapes span several 128-key tiles with ragged tails, one and two query tiles
+per unit, GQA groups 1..8, head_dim 64 and 128, BeamKV depth t = 1 and 2,
+and several requests sharing one ContextKV pool.  Tolerance:
+|gpu - ref| <= 1e-2 + 1e-2*|ref| (bf16 K/V, fp32 accumulate).
+"""
+import pytest
+
+from tests.harness import LockStep, Spec
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(spec, steps=1):
+    ls = LockStep(spec)
+    ls.topk_step()
+    out = []
+    for t in range(1, steps + 1):
+        for layer in range(spec.n_layers):
+            out.append(ls.attention(layer))
+        if t < steps:
+            ls.topk_step()
+    return ls, out
+
+
+@pytest.mark.parametrize("T", [1, 127, 128, 129, 1000])
+@pytest.mark.parametrize("D", [64, 128])
+def test_context_lengths(T, D):
+    spec = Spec(n_q_heads=4, n_kv_heads=2, head_dim=D, vocab=2048, n_levels=2, codes_per_level=64,
+                code_base=1024, ctx_lens=[T], widths=[48], n_items=[2000], seed=T + D)
+    _, res = _run(spec)
+    assert max(r["worst"] for r in res) <= 1.0, res
+
+
+@pytest.mark.parametrize("G,W", [(1, 256), (2, 200), (4, 64), (8, 16), (2, 256)])
+def test_groups_and_widths(G, W):
+    Hkv = 2
+    spec = Spec(n_q_heads=G * Hkv, n_kv_heads=Hkv, head_dim=128, vocab=2048, n_levels=2, codes_per_level=256,
+                code_base=1024, ctx_lens=[777], widths=[W], n_items=[60000], seed=G * 1000 + W)
+    _, res = _run(spec)
+    assert max(r["worst"] for r in res) <= 1.0, res
+
+
+def test_two_beam_levels_many_requests():
+    spec = Spec(n_layers=3, n_q_heads=16, n_kv_heads=8, head_dim=128, vocab=8192, n_levels=3,
+                codes_per_level=128, code_base=8192 - 384, ctx_lens=[300, 1, 513, 2048],
+                widths=[30, 5, 128, 256], n_items=[8000] * 4, seed=11)
+    _, res = _run(spec, steps=2)
+    assert max(r["worst"] for r in res) <= 1.0, res
+
+
+def test_layers_are_independent():
+    # the same layer called at the next step after an advance; layer order reversed
+    spec = Spec(n_layers=4, n_q_heads=4, n_kv_heads=1, head_dim=64, vocab=1024, n_levels=3,
+                codes_per_level=16, code_base=512, ctx_lens=[200], widths=[32], n_items=[1500], seed=12)
+    ls = LockStep(spec)
+    ls.topk_step()
+    worst = 0.0
+    for layer in [3, 1, 0, 2]:
+        worst = max(worst, ls.attention(layer)["worst"])
+    ls.topk_step()
+    for layer in [0, 2, 1, 3]:
+        worst = max(worst, ls.attention(layer)["worst"])
+    assert worst <= 1.0

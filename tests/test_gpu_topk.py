@@ -1,0 +1,85 @@
+"""gr_constrained_topk + gr_beam_advance against the oracle step.
+
+Bit-exact selections / BeamPath under the float32 key contract (the oracle's
+LSE passed as lse_in); with the GPU's own LSE: LSE and log-probabilities within
+1e-4 and identical selections (no near-ties on these seeds).  Edge cases: exact
+ties within and across beams, one valid code per prefix, width above the number
+of candidates, width 1, 1024-wide beams, vocab rows with padding.
+"""
+import numpy as np
+import pytest
+
+from tests.harness import LP_TOL, LockStep, Spec
+
+pytestmark = pytest.mark.gpu
+
+
+def test_default_lse_mode_tolerances():
+    spec = Spec(n_q_heads=2, n_kv_heads=1, head_dim=64, vocab=151936, n_levels=3, codes_per_level=256,
+                code_base=151936 - 768, ctx_lens=[8, 8, 8], widths=[256, 100, 33], n_items=[50000] * 3, seed=21)
+    ls = LockStep(spec)
+    r = ls.topk_step(lse_mode=False)
+    assert r["lse_err"] <= LP_TOL and r["lp_err"] <= LP_TOL, r
+    assert not r["mismatch"], r
+    ls2 = LockStep(spec)
+    ls2.topk_step(lse_mode=True)
+    r = ls2.topk_step(lse_mode=False)
+    assert r["lse_err"] <= LP_TOL and r["lp_err"] <= LP_TOL, r
+    assert not r["mismatch"], r
+
+
+def _ties(ls, t, x):
+    # exact ties: quantised logits, and duplicate rows for pairs of beams
+    x = np.round(x * 2.0) / 2.0
+    rows = ls.beam.rows
+    for b in range(0, rows - 1, 2):
+        x[b + 1] = x[b]
+    return x
+
+
+@pytest.mark.parametrize("W", [1, 5, 64, 256])
+def test_exact_ties(W):
+    spec = Spec(n_q_heads=2, n_kv_heads=1, head_dim=64, vocab=4096, n_levels=3, codes_per_level=64,
+                code_base=4096 - 192, ctx_lens=[8, 8], widths=[W, W], n_items=[5000, 5000], seed=22 + W)
+    ls = LockStep(spec, logits_fn=_ties)
+    for t in range(3):
+        r = ls.topk_step(lse_mode=True)
+        assert not r["mismatch"], (t, r)
+
+
+def test_one_child_per_prefix():
+    # every item has a unique first code: after level 0 each beam has one valid code
+    C = 64
+    items = np.stack([np.arange(C), np.random.default_rng(0).integers(0, C, C)], axis=1).astype(np.int32)
+    spec = Spec(vocab=1024, n_levels=2, codes_per_level=C, code_base=512, widths=[16], n_items=[C], seed=23)
+    ls = LockStep.__new__(LockStep)
+    import tests.harness as H
+    orig = H.make_items
+    H.make_items = lambda s: [items]
+    try:
+        ls.__init__(spec)
+    finally:
+        H.make_items = orig
+    for t in range(2):
+        r = ls.topk_step(lse_mode=True)
+        assert not r["mismatch"], (t, r)
+        assert r["n_sel"] == [16]
+
+
+def test_wide_beam_1024():
+    spec = Spec(n_q_heads=2, n_kv_heads=1, head_dim=64, vocab=8192, n_levels=2, codes_per_level=512,
+                code_base=8192 - 1024, ctx_lens=[4], widths=[1024], n_items=[200000], seed=24)
+    ls = LockStep(spec)
+    for t in range(2):
+        r = ls.topk_step(lse_mode=True)
+        assert not r["mismatch"], (t, r)
+        assert r["n_sel"][0] == min(1024, r["n_sel"][0])
+
+
+def test_single_level_catalogue():
+    spec = Spec(vocab=1024, n_levels=1, codes_per_level=100, code_base=0, widths=[10, 200],
+                ctx_lens=[4, 4], n_items=[60, 60], seed=25)
+    ls = LockStep(spec)
+    r = ls.topk_step(lse_mode=True)
+    assert not r["mismatch"], r
+    assert r["n_sel"] == [10, 60]
