@@ -729,8 +729,8 @@ extern "C" gr_status gr_beam_advance(gr_beam* h, gr_stream_t stream) {
 
 extern "C" gr_status gr_beam_rewind(gr_beam* h, int step) {
     if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
-    if (step < 1 || step > h->step)
-        return fail(GR_ERR_STATE, "can rewind only to a decoded step 1..%d (asked %d)", h->step, step);
+    if (step < 0 || step > h->step)
+        return fail(GR_ERR_STATE, "can rewind only to a decoded step 0..%d (asked %d)", h->step, step);
     h->step = step;
     h->topk_done = false;
     std::fill(h->attn_done.begin(), h->attn_done.end(), 0);

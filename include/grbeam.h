@@ -191,9 +191,9 @@ gr_status gr_constrained_topk(gr_beam* beam, const float* logits, int64_t ld, fl
  * step counter becomes t+1. */
 gr_status gr_beam_advance(gr_beam* beam, gr_stream_t stream);
 
-/* Set the step counter back to `step` (1 <= step <= current step) so that
+/* Set the step counter back to `step` (0 <= step <= current step) so that
  * step `step` can be decoded again from the BeamPath levels before it (host
- * state only; nothing is enqueued). */
+ * state only; nothing is enqueued).  Step 0 starts again from the root beam. */
 gr_status gr_beam_rewind(gr_beam* beam, int step);
 
 /* All surviving beams of request `request` after the last step, best first

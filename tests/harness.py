@@ -206,7 +206,9 @@ class LockStep:
             if not lse_mode:
                 res["lse_err"] = max(res["lse_err"], float(np.max(np.abs(lse_g[r0:r0 + n] - np.array(info["lse64"])))))
                 ref_lp = info["logprobs"]
-                fin = np.isfinite(ref_lp)
+                fin = np.zeros(ref_lp.shape, dtype=bool)  # valid (beam, code) pairs per the oracle's trie
+                for (_, _, b, c) in info["candidates"]:
+                    fin[b, c] = True
                 got = lp_g[r0:r0 + n]
                 if not np.array_equal(np.isfinite(got), fin):
                     res["lp_err"] = float("inf")
