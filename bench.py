@@ -394,8 +394,13 @@ def main():
     ap.add_argument("--impl", default="gr", choices=["gr", "reference"])
     ap.add_argument("--workload", default="long", choices=["tiny", "page1", "short", "long", "mixed"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="keep only the first N requests of the workload (a smaller case for profiling)")
     args = ap.parse_args()
     w = wl.make_workload(args.workload)
+    if args.requests:
+        n = args.requests
+        w.ctx_lens, w.beam_widths, w.n_items = w.ctx_lens[:n], w.beam_widths[:n], w.n_items[:n]
     if args.impl == "reference":
         return run_reference(args, w)
     from beam_decode_gb300.build import build
