@@ -24,6 +24,7 @@ GR_ERR_STATE = -4
 GR_ERR_CUDA = -5
 GR_ERR_TIMEOUT = -6
 GR_ERR_DEVICE = -7
+GR_NOALLOC_MAX_CANDIDATES = 256 * 1024
 
 KERNEL_CTX_ATTN = 0
 KERNEL_BEAM_ATTN = 1
@@ -42,7 +43,7 @@ SYMBOLS = [
     "gr_beam_rows", "gr_beam_step", "gr_beam_kv_slot", "gr_decode_attn", "gr_constrained_topk",
     "gr_beam_advance", "gr_beam_rewind", "gr_beam_results", "gr_beam_path", "gr_beam_status",
     "gr_beam_set_timing", "gr_beam_kernel_stats", "gr_beam_set_wait_limit",
-    "gr_status_str", "gr_last_error",
+    "gr_constrained_topk_noalloc", "gr_status_str", "gr_last_error",
 ]
 
 
@@ -101,6 +102,8 @@ def lib() -> ctypes.CDLL:
             "gr_beam_set_timing": [vp, c_int],
             "gr_beam_kernel_stats": [vp, c_int, P(c_i64), P(ctypes.c_double), c_int],
             "gr_beam_set_wait_limit": [vp, c_i64],
+            "gr_constrained_topk_noalloc": [vp, c_i64, c_int, c_int, c_int, c_int, vp, vp, c_int, vp, vp, vp, vp,
+                                            vp],
             "gr_status_str": [c_int],
             "gr_last_error": [],
         }

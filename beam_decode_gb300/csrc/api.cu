@@ -96,6 +96,19 @@ int device_sm_count() {
 }
 }  // namespace
 
+namespace grb {
+// error reporting for entry points defined in other translation units
+gr_status set_error(gr_status code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+}  // namespace grb
+
 // ---------------------------------------------------------------------------
 // trie
 // ---------------------------------------------------------------------------

@@ -248,6 +248,48 @@ gr_status gr_beam_kernel_stats(gr_beam* beam, int kind, int64_t* launches, doubl
  * pipeline wait give up on its first check, for fault-path tests. */
 gr_status gr_beam_set_wait_limit(gr_beam* beam, int64_t nanoseconds);
 
+/* ------------------------------------------------------------------------ */
+/* Constrained top-K without caller-provided scratch                         */
+/* ------------------------------------------------------------------------ */
+
+/* The pages have no counterpart to this entry point; it serves callers that
+ * cannot allocate device memory -- plugins of an inference server that are
+ * handed only their input and output tensors, or services whose device
+ * memory is budgeted once at start-up and must not grow per request.  They
+ * cannot create a gr_beam handle, whose workspace the caller allocates.
+ *
+ * It computes, for ONE request, what gr_constrained_topk computes: the
+ * full-vocabulary log-sum-exp LSE_b of each row, key(b, c) = S_b +
+ * (x[b][code_lo + c] - LSE_b) (float32, each operation rounded once) over the
+ * codes c whose bit is set in the row's mask, ordered by key descending then
+ * flat index b*n_codes + c ascending; the first min(k, #candidates) are
+ * written.  NaN keys are not candidates.  Identical inputs give the same
+ * selection and keys as gr_constrained_topk.
+ *   logits       device fp32 [n_rows][ld], ld >= vocab, ld % 4 == 0, 16-byte aligned
+ *   beam_scores  device fp32 [n_rows] (S_b), or NULL for all zero
+ *   valid_mask   device uint32 [n_rows][ceil(n_codes/32)]: bit c of row b set
+ *                when code c may follow beam b's prefix
+ *   out_parent, out_code  device int32 [k]; out_key device fp32 [k];
+ *   out_n        device int32 [1]: number written
+ * Limits: n_rows * n_codes <= GR_NOALLOC_MAX_CANDIDATES, n_codes <= 1024,
+ * k <= 1024; larger sizes return GR_ERR_CAPACITY and launch nothing.
+ * Scratch: the candidate keys live in one fixed device array of the library
+ * (GR_NOALLOC_MAX_CANDIDATES x 4 bytes = 1 MiB) that every GPU which loads
+ * the library holds until the process exits.  The call allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.  Every call on
+ * a device shares that one array and overwrites it completely, so calls that
+ * overlap on the GPU (concurrent streams, or several host threads) race and
+ * must be serialised by the caller; calls queued on one stream are fine.
+ * The first call on each device looks the array's device address up
+ * (cudaGetSymbolAddress with that device current); make that first call
+ * before any stream capture on that device.  Enqueues two kernels on
+ * `stream` and returns without synchronising. */
+#define GR_NOALLOC_MAX_CANDIDATES (256 * 1024)
+gr_status gr_constrained_topk_noalloc(const float* logits, int64_t ld, int n_rows, int vocab, int code_lo,
+                                      int n_codes, const float* beam_scores, const uint32_t* valid_mask, int k,
+                                      int32_t* out_parent, int32_t* out_code, float* out_key, int32_t* out_n,
+                                      gr_stream_t stream);
+
 const char* gr_status_str(gr_status status);
 const char* gr_last_error(void);
 
