@@ -151,6 +151,58 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// all 128 columns of this warp's 32 lanes in one round trip (128 registers per thread)
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : GRB_R8(0), GRB_R8(8), GRB_R8(16), GRB_R8(24), GRB_R8(32), GRB_R8(40), GRB_R8(48), GRB_R8(56),
+          GRB_R8(64), GRB_R8(72), GRB_R8(80), GRB_R8(88), GRB_R8(96), GRB_R8(104), GRB_R8(112), GRB_R8(120)
+        : "r"(taddr)
+        : "memory");
+}
+
+// packed fp32 pairs (Blackwell f32x2 ALU)
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// CTA-wide named barrier (all 384 threads), usable from separate code regions
+__device__ __forceinline__ void named_bar_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(384) : "memory");
+}
+
+// register split between warpgroups (sums to the launch's 384 x 168)
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
 // Shared-memory matrix descriptor, 128-byte swizzle, descriptor version 1.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
@@ -180,7 +232,7 @@ struct Waiter {
 };
 
 // one thread
-__device__ __noinline__ bool wait1(uint32_t bar, uint32_t parity, const Waiter& w) {
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const Waiter w) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = global_timer();
     uint32_t spins = 0;
@@ -198,7 +250,7 @@ __device__ __noinline__ bool wait1(uint32_t bar, uint32_t parity, const Waiter& 
 }
 
 // whole warp (convergent): returns the same value on every lane
-__device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Waiter& w) {
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Waiter w) {
     const int lane = threadIdx.x & 31;
     uint64_t t0 = 0;
     uint32_t spins = 0;
@@ -222,7 +274,7 @@ __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Wait
 }
 
 // drain: fixed limit, no abort check
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     uint64_t t0 = global_timer();
     while (!mbar_try_wait(bar, parity)) {
         if ((int64_t)(global_timer() - t0) > kDrainLimitNs) return;
@@ -299,15 +351,16 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
     const int2 jr = st.cta_jobs[blockIdx.x];
     const Waiter wt{wait_limit_ns, abort_flag, st.status};
 
-    // producer state (kept for the drain)
-    uint32_t p_kit = 0, p_vit = 0, p_qcnt = 0;
-    // MMA state
-    bool mma_issued = false;
-
+    // The producer / MMA / allocator warpgroup gives registers to the two softmax
+    // warpgroups (128 x 56 + 2 x 128 x 224 = 384 x 168).  The two register
+    // regions never rejoin: each side runs its own teardown and returns.
+    if (warp < 4) {
+        regs_dec<56>();
+        // producer state (kept for the drain)
+        uint32_t p_kit = 0, p_vit = 0, p_qcnt = 0;
     if (warp == 0) {
         if (lane == 0) {
             bool ok = true;
@@ -350,6 +403,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
+            bool mma_issued = false;
             constexpr uint32_t idesc_s = idesc_bf16(128, kTileKeys, false);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, true);
             uint32_t kit = 0, vit = 0, qcnt = 0;
@@ -434,7 +488,28 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    }
+        tc_fence_before();
+        named_bar_sync(1);
+        // after an abort, every copy the producer issued must land before the CTA exits
+        if (warp == 0 && lane == 0 && *abort_flag) {
+            if (p_qcnt > 0) wait_drain(bar(B_Q_FULL), (p_qcnt - 1) & 1);
+            for (int s = 0; s < 2; ++s) {
+                const uint32_t nk = (p_kit + 1 - s) / 2;  // issues into stage s
+                if (nk > 0) wait_drain(bar(B_K_FULL + s), (nk - 1) & 1);
+                const uint32_t nv = (p_vit + 1 - s) / 2;
+                if (nv > 0) wait_drain(bar(B_V_FULL + s), (nv - 1) & 1);
+            }
+        }
+        __syncwarp();
+        named_bar_sync(2);
+        tc_fence_after();
+        if (warp == 2) tmem_dealloc(tmem, P::kTmemCols);
+        return;
+    }
+
+    regs_inc<224>();
+    {
         // softmax warpgroups
         const int i = (warp - 4) >> 2;          // query tile of this warpgroup
         const int quarter = warp & 3;           // TMEM lane quarter
@@ -453,17 +528,23 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
                 if (!(ok = wait_warp(bar(B_S_FULL + i), tiles & 1, wt))) break;
                 tc_fence_after();
                 uint32_t sv[128];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + P::s_col(i) + 32 * c, sv + 32 * c);
+                tmem_ld128(tmem + lane_base + P::s_col(i), sv);
                 const int valid = ctx_len - (J.t0 + jj) * kTileKeys;
                 if (valid < kTileKeys) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (c >= valid) sv[c] = __float_as_uint(-CUDART_INF_F);
                 }
-                float mx = -CUDART_INF_F;
+                // row maximum: four independent 3-input max chains
+                float a0 = -CUDART_INF_F, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+                for (int c = 0; c < 128; c += 8) {
+                    a0 = fmax3(a0, __uint_as_float(sv[c + 0]), __uint_as_float(sv[c + 1]));
+                    a1 = fmax3(a1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+                    a2 = fmax3(a2, __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+                    a3 = fmax3(a3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+                }
+                const float mx = fmax3(fmaxf(a0, a1), a2, a3);
                 if (jj == 0) {
                     m_used = mx;
                 } else {
@@ -485,16 +566,25 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
                         m_used = m_new;
                     }
                 }
-                const float mb = m_used * scale_log2;
-                float lsum = 0.f;
+                // p = 2^(s*scale_log2 - m*scale_log2), two columns per packed FMA
+                const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+                const uint64_t mb2 = f2_pack(-m_used * scale_log2, -m_used * scale_log2);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
-                    const float p0 = exp2f(fmaf(__uint_as_float(sv[2 * c]), scale_log2, -mb));
-                    const float p1 = exp2f(fmaf(__uint_as_float(sv[2 * c + 1]), scale_log2, -mb));
-                    lsum += p0 + p1;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), sc2, mb2),
+                              x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
                     sv[c] = pack_bf16x2(p0, p1);
                 }
-                l += lsum;
+                float s0, s1, s2, s3, s4, s5, s6, s7;
+                f2_unpack(acc[0], s0, s1);
+                f2_unpack(acc[1], s2, s3);
+                f2_unpack(acc[2], s4, s5);
+                f2_unpack(acc[3], s6, s7);
+                l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
                 tmem_st32(tmem + lane_base + P::p_col(i), sv);
                 tmem_st32(tmem + lane_base + P::p_col(i) + 32, sv + 32);
                 tmem_st_wait();
@@ -525,22 +615,9 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
             ++jobs;
         }
     }
-
     tc_fence_before();
-    __syncthreads();
-    // after an abort, every copy the producer issued must land before the CTA exits
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        if (p_qcnt > 0) wait_drain(bar(B_Q_FULL), (p_qcnt - 1) & 1);
-        for (int s = 0; s < 2; ++s) {
-            const uint32_t nk = (p_kit + 1 - s) / 2;  // issues into stage s
-            if (nk > 0) wait_drain(bar(B_K_FULL + s), (nk - 1) & 1);
-            const uint32_t nv = (p_vit + 1 - s) / 2;
-            if (nv > 0) wait_drain(bar(B_V_FULL + s), (nv - 1) & 1);
-        }
-    }
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 2) tmem_dealloc(tmem, P::kTmemCols);
+    named_bar_sync(1);
+    named_bar_sync(2);
 }
 
 // ---------------------------------------------------------------------------
