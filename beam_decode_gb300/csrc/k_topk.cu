@@ -14,7 +14,8 @@
 //                        key = S_b + (x - LSE_b), stored as order-preserving
 //                        uint32 (0 = not a candidate).  HBM-bound.
 //   k_topk_select        per request: radix select of the W-th largest key over
-//                        n_live*C candidates (12/12/8-bit digits), ties at the
+//                        n_live*C candidates (13/11/8-bit digits, the threshold
+//                        digit compacted into shared memory), ties at the
 //                        threshold taken in flat-index order, then a bitonic
 //                        sort of the survivors by (key desc, flat asc).
 //   k_advance            BeamPath commit: parent, token, trie node, score,
@@ -25,6 +26,7 @@
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
+#include <limits.h>
 #include <stdint.h>
 
 #include "grbeam_internal.h"
@@ -183,8 +185,30 @@ k_logsoftmax_gather(GrState st, int t, const float* __restrict__ logits, int64_t
 // ---------------------------------------------------------------------------
 // K4: cross-beam top-K of one request
 // ---------------------------------------------------------------------------
+// Keys are order-preserving uint32 (0 = not a candidate); the flat index of a
+// candidate is its position b*C + c in the request's key array.  The k-th
+// largest key tau is found digit by digit (13 bits, then 11, then 8):
+//   A  one pass over all keys: histogram of the top 13 bits;
+//   B  one pass: keys above the threshold digit go straight to the output
+//      set, keys in the threshold digit are compacted into shared memory;
+//   C  the remaining 19 bits are resolved on the compacted keys;
+//   D  keys above tau are taken, keys equal to tau in flat-index order;
+// then the survivors are sorted by (key desc, flat asc) with a bitonic network.
+// If the threshold digit holds more than kSelCap keys, B-D run on global
+// memory instead (three histogram passes over all keys).
 constexpr int kSelThreads = 1024;
-constexpr int kHistBins = 4096;
+constexpr int kBinsA = 8192;    // top digit: sign, exponent, 4 mantissa bits
+constexpr int kShiftA = 19;
+constexpr int kSelCap = 4096;   // compacted threshold-digit keys kept in shared memory
+
+struct SelSmem {
+    int hist[kBinsA];
+    uint32_t ck[kSelCap];       // compacted keys of the threshold digit
+    uint32_t ci[kSelCap];       // their flat indices
+    unsigned long long sel[kMaxBeam];
+    int warp_tot[32];
+    int digit, kk, count, n_sel, n_c;
+};
 
 // inclusive prefix sum over the block in thread order; returns the block total
 __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot, int& total) {
@@ -212,7 +236,94 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot, int& total)
     return v + add;
 }
 
+// digit d of the kk-th largest element given a histogram of nbins bins:
+// sum(bins > d) < kk <= sum(bins >= d); writes sm.digit and sm.kk (kk within d)
+__device__ __forceinline__ void find_digit(SelSmem& sm, int nbins, int kk) {
+    const int tid = threadIdx.x;
+    const int per = nbins > kSelThreads ? nbins / kSelThreads : 1;
+    const bool owner = tid < nbins / per;
+    const int hi = nbins - 1 - tid * per;  // thread order = descending bin order
+    int v = 0;
+    if (owner)
+        for (int e = 0; e < per; ++e) v += sm.hist[hi - e];
+    int total;
+    const int incl = block_incl_scan(v, sm.warp_tot, total);
+    const int excl = incl - v;
+    if (owner && excl < kk && kk <= incl) {
+        int acc = excl;
+        for (int e = 0; e < per; ++e) {
+            const int h = sm.hist[hi - e];
+            if (acc + h >= kk) { sm.digit = hi - e; sm.kk = kk - acc; break; }
+            acc += h;
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ unsigned long long sel_entry(uint32_t u, uint32_t flat) {
+    return ((unsigned long long)u << 32) | (unsigned)(0xFFFFFFFFu - flat);
+}
+
+// warp-aggregated histogram add of `bin` for lanes with q set (all lanes call)
+__device__ __forceinline__ void hist_add(int* hist, bool q, uint32_t bin) {
+    if (__any_sync(0xffffffffu, q)) {
+        const unsigned peers = __match_any_sync(0xffffffffu, q ? bin : 0xFFFFFFFFu);
+        if (q && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(peers));
+    }
+}
+
+// B-D on global memory, for a threshold digit too full for shared memory:
+// two more histogram passes over all keys, then the gather
+__device__ void select_global(SelSmem& sm, const uint32_t* keys, int N, uint32_t prefix, uint32_t pmask, int kk,
+                              int k_want) {
+    const int tid = threadIdx.x;
+    const int shifts[2] = {8, 0};
+    const int widths[2] = {11, 8};
+    for (int pass = 0; pass < 2; ++pass) {
+        const int sh = shifts[pass];
+        const uint32_t dmask = (1u << widths[pass]) - 1u;
+        for (int i = tid; i < kBinsA; i += kSelThreads) sm.hist[i] = 0;
+        __syncthreads();
+        for (int base = 0; base < N; base += kSelThreads) {
+            const int i = base + tid;
+            const uint32_t u = (i < N) ? keys[i] : 0u;
+            const bool q = (u != 0) && ((u & pmask) == prefix);
+            hist_add(sm.hist, q, (u >> sh) & dmask);
+        }
+        __syncthreads();
+        find_digit(sm, 1 << widths[pass], kk);
+        prefix |= (uint32_t)sm.digit << sh;
+        pmask |= dmask << sh;
+        kk = sm.kk;
+    }
+    const uint32_t tau = prefix;
+    const int n_eq = sm.hist[sm.digit];
+    __syncthreads();
+    for (int i = tid; i < N; i += kSelThreads) {
+        const uint32_t u = keys[i];
+        if (u > tau || (n_eq == kk && u == tau)) sm.sel[atomicAdd(&sm.n_sel, 1)] = sel_entry(u, (uint32_t)i);
+    }
+    __syncthreads();
+    if (n_eq != kk) {  // ties at the threshold: the kk smallest flat indices
+        int base_rank = 0;
+        for (int start = 0; start < N; start += kSelThreads) {
+            const int i = start + tid;
+            const int e = (i < N && keys[i] == tau) ? 1 : 0;
+            int total;
+            const int incl = block_incl_scan(e, sm.warp_tot, total);
+            const int rank = base_rank + incl - e;
+            if (e && rank < kk) sm.sel[atomicAdd(&sm.n_sel, 1)] = sel_entry(tau, (uint32_t)i);
+            base_rank += total;
+            if (base_rank >= kk) break;
+        }
+        __syncthreads();
+    }
+    (void)k_want;
+}
+
 __global__ void __launch_bounds__(kSelThreads) k_topk_select(GrState st, int t) {
+    extern __shared__ __align__(16) uint8_t sel_smem_raw[];
+    SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_smem_raw);
     const int r = blockIdx.x;
     const GrReqDev R = st.req[r];
     if (t >= R.n_levels) return;
@@ -221,124 +332,140 @@ __global__ void __launch_bounds__(kSelThreads) k_topk_select(GrState st, int t) 
     const int N = n_live * C;
     const uint32_t* keys = st.cand + (int64_t)R.row_off * C;
     const int k_want = R.width;
-
-    __shared__ int hist[kHistBins];
-    __shared__ int warp_tot[32];
-    __shared__ int sh_digit, sh_kk, sh_count, sh_gt, sh_eqcnt;
-    __shared__ unsigned long long sel[kMaxBeam];
-
     const int tid = threadIdx.x;
-    // pass 0: count candidates + histogram of bits [31:20]
-    uint32_t prefix = 0, pmask = 0;
-    int kk = k_want;
-    int n_valid = 0;
-    const int shifts[3] = {20, 8, 0};
-    const int widths[3] = {12, 12, 8};
-    bool take_all = false;
-    for (int pass = 0; pass < 3; ++pass) {
-        const int sh = shifts[pass];
-        const uint32_t dmask = (1u << widths[pass]) - 1u;
-        for (int i = tid; i < kHistBins; i += kSelThreads) hist[i] = 0;
-        if (tid == 0) sh_count = 0;
-        __syncthreads();
-        int my_valid = 0;
-        // every lane runs the same trip count so the warp is converged at the match
-        for (int base = 0; base < N; base += kSelThreads) {
-            const int i = base + tid;
-            const uint32_t u = (i < N) ? keys[i] : 0u;
-            const bool q = (u != 0) && ((u & pmask) == prefix);
-            my_valid += (u != 0);
-            const uint32_t bin = q ? ((u >> sh) & dmask) : 0xFFFFFFFFu;
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (q && (__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[bin], __popc(peers));
-        }
-        if (pass == 0) {
-            atomicAdd(&sh_count, my_valid);
-            __syncthreads();
-            n_valid = sh_count;
-            if (n_valid <= k_want) { take_all = true; break; }
-        }
-        __syncthreads();
-        // thread j owns bins [nb*(T-1-j), nb*(T-j)) so thread order = descending bin order
-        const int nbins = 1 << widths[pass];
-        const int per = nbins / kSelThreads > 0 ? nbins / kSelThreads : 1;
-        const int owner_active = (tid < nbins / per);
-        int hi = nbins - 1 - tid * per;  // highest bin of this thread
-        int v = 0;
-        if (owner_active)
-            for (int e = 0; e < per; ++e) v += hist[hi - e];
-        int total;
-        const int incl = block_incl_scan(v, warp_tot, total);
-        const int excl = incl - v;
-        if (owner_active && excl < kk && kk <= incl) {
-            int acc = excl;
-            for (int e = 0; e < per; ++e) {
-                const int h = hist[hi - e];
-                if (acc + h >= kk) { sh_digit = hi - e; sh_kk = kk - acc; break; }
-                acc += h;
-            }
-        }
-        __syncthreads();
-        prefix |= (uint32_t)sh_digit << sh;
-        pmask |= dmask << sh;
-        kk = sh_kk;
-        if (pass == 2 && tid == 0) sh_eqcnt = hist[sh_digit];  // keys equal to the threshold
-        __syncthreads();
-    }
 
-    // gather: all keys > tau, plus the first kk keys == tau in flat order
-    const uint32_t tau = take_all ? 0u : prefix;
-    if (tid == 0) sh_gt = 0;
+    // A: histogram of the top digit and the number of candidates
+    for (int i = tid; i < kBinsA; i += kSelThreads) sm.hist[i] = 0;
+    if (tid == 0) { sm.count = 0; sm.n_sel = 0; sm.n_c = 0; }
     __syncthreads();
-    const bool eq_all = take_all || (sh_eqcnt == kk);
-    const int n_take = take_all ? n_valid : k_want;
-    for (int i = tid; i < N; i += kSelThreads) {
-        const uint32_t u = keys[i];
-        const bool pick = take_all ? (u != 0) : (u > tau || (eq_all && u == tau));
-        if (pick) {
-            const int pos = atomicAdd(&sh_gt, 1);
-            sel[pos] = ((unsigned long long)u << 32) | (unsigned)(0xFFFFFFFFu - (uint32_t)i);
+    int my_valid = 0;
+    for (int base = 0; base < N; base += 4 * kSelThreads) {
+        uint32_t u[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = base + k * kSelThreads + tid;
+            u[k] = (i < N) ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            my_valid += (u[k] != 0);
+            hist_add(sm.hist, u[k] != 0, u[k] >> kShiftA);
         }
     }
+    atomicAdd(&sm.count, my_valid);
     __syncthreads();
-    if (!eq_all) {
-        // ties at the threshold: keep the kk smallest flat indices, in index order
-        int base_rank = 0;
-        for (int start = 0; start < N; start += kSelThreads) {
-            const int i = start + tid;
-            const int e = (i < N && keys[i] == tau) ? 1 : 0;
-            int total;
-            const int incl = block_incl_scan(e, warp_tot, total);
-            const int rank = base_rank + incl - e;
-            if (e && rank < kk) {
-                const int pos = atomicAdd(&sh_gt, 1);
-                sel[pos] = ((unsigned long long)tau << 32) | (unsigned)(0xFFFFFFFFu - (uint32_t)i);
-            }
-            base_rank += total;
-            if (base_rank >= kk) break;
+    const int n_valid = sm.count;
+    int n_take;
+    if (n_valid <= k_want) {
+        // every candidate survives
+        for (int i = tid; i < N; i += kSelThreads) {
+            const uint32_t u = keys[i];
+            if (u != 0) sm.sel[atomicAdd(&sm.n_sel, 1)] = sel_entry(u, (uint32_t)i);
         }
+        n_take = n_valid;
+    } else {
+        find_digit(sm, kBinsA, k_want);
+        const uint32_t dA = (uint32_t)sm.digit;
+        int kk = sm.kk;
+        const int cnt_a = sm.hist[dA];
         __syncthreads();
+        n_take = k_want;
+        if (cnt_a <= kSelCap) {
+            // B: above the digit -> output set; the digit itself -> shared memory
+            for (int i = tid; i < N; i += kSelThreads) {
+                const uint32_t u = keys[i];
+                if (u == 0) continue;
+                const uint32_t d = u >> kShiftA;
+                if (d > dA) {
+                    sm.sel[atomicAdd(&sm.n_sel, 1)] = sel_entry(u, (uint32_t)i);
+                } else if (d == dA) {
+                    const int pos = atomicAdd(&sm.n_c, 1);
+                    sm.ck[pos] = u;
+                    sm.ci[pos] = (uint32_t)i;
+                }
+            }
+            __syncthreads();
+            const int n_c = sm.n_c;
+            // C: the remaining 19 bits on the compacted keys
+            uint32_t prefix = dA << kShiftA, pmask = ~((1u << kShiftA) - 1u);
+            const int shifts[2] = {8, 0};
+            const int widths[2] = {11, 8};
+            for (int pass = 0; pass < 2; ++pass) {
+                const int sh = shifts[pass];
+                const uint32_t dmask = (1u << widths[pass]) - 1u;
+                for (int i = tid; i < (1 << widths[pass]); i += kSelThreads) sm.hist[i] = 0;
+                __syncthreads();
+                for (int e = tid; e < n_c; e += kSelThreads) {
+                    const uint32_t u = sm.ck[e];
+                    if ((u & pmask) == prefix) atomicAdd(&sm.hist[(u >> sh) & dmask], 1);
+                }
+                __syncthreads();
+                find_digit(sm, 1 << widths[pass], kk);
+                prefix |= (uint32_t)sm.digit << sh;
+                pmask |= dmask << sh;
+                kk = sm.kk;
+            }
+            const uint32_t tau = prefix;
+            const int n_eq = sm.hist[sm.digit];
+            __syncthreads();
+            // D: above tau, then ties at tau in flat-index order
+            if (tid == 0) sm.count = 0;
+            __syncthreads();
+            for (int e = tid; e < n_c; e += kSelThreads) {
+                const uint32_t u = sm.ck[e];
+                if (u > tau || (n_eq == kk && u == tau)) {
+                    sm.sel[atomicAdd(&sm.n_sel, 1)] = sel_entry(u, sm.ci[e]);
+                } else if (u == tau) {
+                    sm.hist[atomicAdd(&sm.count, 1)] = (int)sm.ci[e];  // tie indices
+                }
+            }
+            __syncthreads();
+            if (n_eq != kk) {
+                int P = 1;
+                while (P < n_eq) P <<= 1;
+                for (int e = n_eq + tid; e < P; e += kSelThreads) sm.hist[e] = INT_MAX;
+                __syncthreads();
+                for (int k = 2; k <= P; k <<= 1) {  // ascending sort of the tie indices
+                    for (int j = k >> 1; j > 0; j >>= 1) {
+                        for (int e = tid; e < P; e += kSelThreads) {
+                            const int ex = e ^ j;
+                            if (ex > e) {
+                                const int a = sm.hist[e], c = sm.hist[ex];
+                                if (((e & k) == 0) ? (a > c) : (a < c)) { sm.hist[e] = c; sm.hist[ex] = a; }
+                            }
+                        }
+                        __syncthreads();
+                    }
+                }
+                for (int e = tid; e < kk; e += kSelThreads)
+                    sm.sel[atomicAdd(&sm.n_sel, 1)] = sel_entry(tau, (uint32_t)sm.hist[e]);
+                __syncthreads();
+            }
+        } else {
+            select_global(sm, keys, N, dA << kShiftA, ~((1u << kShiftA) - 1u), kk, k_want);
+        }
     }
+    __syncthreads();
     // bitonic sort of n_take entries, descending
     int P = 1;
     while (P < n_take) P <<= 1;
-    for (int i = n_take + tid; i < P; i += kSelThreads) sel[i] = 0ull;
+    for (int i = n_take + tid; i < P; i += kSelThreads) sm.sel[i] = 0ull;
     __syncthreads();
     for (int k = 2; k <= P; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
             for (int i = tid; i < P; i += kSelThreads) {
                 const int ixj = i ^ j;
                 if (ixj > i) {
-                    const unsigned long long a = sel[i], c = sel[ixj];
+                    const unsigned long long a = sm.sel[i], c = sm.sel[ixj];
                     const bool desc = ((i & k) == 0);
-                    if (desc ? (a < c) : (a > c)) { sel[i] = c; sel[ixj] = a; }
+                    if (desc ? (a < c) : (a > c)) { sm.sel[i] = c; sm.sel[ixj] = a; }
                 }
             }
             __syncthreads();
         }
     }
     for (int i = tid; i < n_take; i += kSelThreads) {
-        const unsigned long long e = sel[i];
+        const unsigned long long e = sm.sel[i];
         const uint32_t flat = 0xFFFFFFFFu - (uint32_t)(e & 0xFFFFFFFFull);
         st.sel_parent[R.row_off + i] = (int)(flat / (uint32_t)C);
         st.sel_code[R.row_off + i] = (int)(flat % (uint32_t)C);
@@ -428,7 +555,14 @@ cudaError_t launch_logsoftmax_gather(const GrState& st, int t, const float* logi
 }
 
 cudaError_t launch_topk_select(const GrState& st, int t, cudaStream_t s) {
-    k_topk_select<<<st.n_req, kSelThreads, 0, s>>>(st, t);
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)sizeof(SelSmem));
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    k_topk_select<<<st.n_req, kSelThreads, sizeof(SelSmem), s>>>(st, t);
     return cudaGetLastError();
 }
 

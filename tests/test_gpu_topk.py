@@ -83,3 +83,16 @@ def test_single_level_catalogue():
     r = ls.topk_step(lse_mode=True)
     assert not r["mismatch"], r
     assert r["n_sel"] == [10, 60]
+
+
+def test_all_keys_equal_uses_global_path():
+    # constant logits: every candidate key is identical, the threshold digit holds
+    # far more keys than the shared-memory stage keeps, ties resolve by flat index
+    def flat(ls, t, x):
+        return np.zeros_like(x)
+    spec = Spec(n_q_heads=2, n_kv_heads=1, head_dim=64, vocab=4096, n_levels=2, codes_per_level=512,
+                code_base=4096 - 1024, ctx_lens=[4], widths=[1024], n_items=[150000], seed=26)
+    ls = LockStep(spec, logits_fn=flat)
+    for t in range(2):
+        r = ls.topk_step(lse_mode=True)
+        assert not r["mismatch"], (t, r)
