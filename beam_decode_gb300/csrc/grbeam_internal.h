@@ -95,6 +95,7 @@ struct GrState {
     int n_units, n_jobs, n_cta;
     float* o_part;      // [n_jobs][kUnitRows][D]
     float* lse_part;    // [n_jobs][kUnitRows]
+    int4* combine_meta; // [rows][Hkv]: first slot, (slots << 16 | row within the unit), beam, W_r
     const uint16_t* beam_k; // bf16 [NL][L-1][rows][Hkv][D]
     const uint16_t* beam_v;
 

@@ -625,128 +625,171 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_to_f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
 
-// running (max, denominator, weighted sum) of one query head
-template <int E>
-struct Mix {
-    float m, den, acc[E];
-    __device__ __forceinline__ void init() {
-        m = -CUDART_INF_F;
-        den = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    }
-    // add a part whose log-weight is lw and whose (normalised) value is v
-    __device__ __forceinline__ void add(float lw, const float* v) {
-        if (lw > m) {
-            const float a = __expf(m - lw);
-            den *= a;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] *= a;
-            m = lw;
-        }
-        const float w = __expf(lw - m);
-        den += w;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, v[e], acc[e]);
-    }
-};
-
-template <int D, int G>
+template <int D, int G, int TMAX>
 __global__ void __launch_bounds__(256) k_beam_attn(GrState st, int t, int layer, const uint16_t* __restrict__ q,
                                                    uint16_t* __restrict__ out, float scale) {
     constexpr int E = D / 32;  // elements per lane
+    constexpr int kPieces = 3;  // context pieces held in registers (more are streamed)
     const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
-    const int Hkv = st.n_kv_heads, Hq = st.n_q_heads;
+    const int Hkv = st.n_kv_heads, Hq = st.n_q_heads, L = st.n_levels;
+    if (gw >= st.rows * Hkv) return;
     const int row = gw / Hkv, h = gw % Hkv;
-    if (row >= st.rows) return;
+    // round 1: everything that depends only on (row, head)
+    const int4 meta = st.combine_meta[gw];  // first slot, slots << 16 | local row, beam, request width
     const int r = st.row_req[row];
-    const GrReqDev& R = st.req[r];
-    const int b = row - R.row_off;
-    const int L = st.n_levels;
-    const int n_live = st.n_beams[r * (L + 1) + t];
+    const uint16_t* qp = q + ((int64_t)row * Hq + h * G) * D + lane * E;
     uint16_t* o = out + ((int64_t)row * Hq + h * G) * D + lane * E;
-    if (t >= R.n_levels || b >= n_live) {
+    float qv[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if constexpr (E == 4) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(qp + g * D));
+            qv[g][0] = __uint_as_float(u.x << 16); qv[g][1] = __uint_as_float(u.x & 0xFFFF0000u);
+            qv[g][2] = __uint_as_float(u.y << 16); qv[g][3] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+            const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(qp + g * D));
+            qv[g][0] = __uint_as_float(u << 16); qv[g][1] = __uint_as_float(u & 0xFFFF0000u);
+        }
+    }
+    // ancestry row: only written for live beams, so every slot is clamped into the
+    // request's rows before it forms an address (a dead row's result is discarded)
+    const int32_t* path = st.path + ((int64_t)(t - 1) * st.rows + row) * L;
+    const int width = meta.w;
+    int slot[TMAX];
+#pragma unroll
+    for (int j = 0; j < TMAX; ++j) {
+        const int v = (j < t) ? __ldg(path + j) : 0;
+        slot[j] = ((unsigned)v < (unsigned)width) ? v : 0;
+    }
+    // round 2: live width, context pieces, BeamKV rows
+    const int n_live = st.n_beams[r * (L + 1) + t];
+    const int b = meta.z, lr = meta.y & 0xFFFF, first = meta.x, n_slots = meta.y >> 16;
+    float plse[kPieces][G], pv[kPieces][G][E];
+#pragma unroll
+    for (int p = 0; p < kPieces; ++p) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if (p < n_slots) {
+                const int64_t pr = (int64_t)(first + p) * kUnitRows + lr + g;
+                plse[p][g] = __ldg(st.lse_part + pr);
+                const float* op = st.o_part + pr * D + lane * E;
+                if constexpr (E == 4) {
+                    const float4 v4 = __ldg(reinterpret_cast<const float4*>(op));
+                    pv[p][g][0] = v4.x; pv[p][g][1] = v4.y; pv[p][g][2] = v4.z; pv[p][g][3] = v4.w;
+                } else {
+                    const float2 v2 = __ldg(reinterpret_cast<const float2*>(op));
+                    pv[p][g][0] = v2.x; pv[p][g][1] = v2.y;
+                }
+            } else {
+                plse[p][g] = -CUDART_INF_F;
+#pragma unroll
+                for (int e = 0; e < E; ++e) pv[p][g][e] = 0.f;
+            }
+        }
+    }
+    float kf[TMAX][E], vf[TMAX][E];
+#pragma unroll
+    for (int j = 0; j < TMAX; ++j) {
+        if (j < t) {
+            const int64_t kv = (((int64_t)layer * (L - 1) + j) * st.rows + (row - b) + slot[j]) * Hkv + h;
+            const uint16_t* kp = st.beam_k + kv * D + lane * E;
+            const uint16_t* vp = st.beam_v + kv * D + lane * E;
+            if constexpr (E == 4) {
+                const uint2 ku = __ldg(reinterpret_cast<const uint2*>(kp)), vu = __ldg(reinterpret_cast<const uint2*>(vp));
+                kf[j][0] = __uint_as_float(ku.x << 16); kf[j][1] = __uint_as_float(ku.x & 0xFFFF0000u);
+                kf[j][2] = __uint_as_float(ku.y << 16); kf[j][3] = __uint_as_float(ku.y & 0xFFFF0000u);
+                vf[j][0] = __uint_as_float(vu.x << 16); vf[j][1] = __uint_as_float(vu.x & 0xFFFF0000u);
+                vf[j][2] = __uint_as_float(vu.y << 16); vf[j][3] = __uint_as_float(vu.y & 0xFFFF0000u);
+            } else {
+                const uint32_t ku = __ldg(reinterpret_cast<const uint32_t*>(kp));
+                const uint32_t vu = __ldg(reinterpret_cast<const uint32_t*>(vp));
+                kf[j][0] = __uint_as_float(ku << 16); kf[j][1] = __uint_as_float(ku & 0xFFFF0000u);
+                vf[j][0] = __uint_as_float(vu << 16); vf[j][1] = __uint_as_float(vu & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) { kf[j][e] = 0.f; vf[j][e] = 0.f; }
+        }
+    }
+    if (t >= st.req[r].n_levels || b >= n_live) {
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
             for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(o + g * D + e) = 0u;
         return;
     }
-    float qv[G][E];
-    const uint16_t* qp = q + ((int64_t)row * Hq + h * G) * D + lane * E;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int e = 0; e < E; ++e) qv[g][e] = bf16_to_f(qp[g * D + e]);
-
-    Mix<E> mix[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) mix[g].init();
-
-    // context partials of the unit holding this beam
-    const int bpu = kUnitRows / G;
-    const GrAttnUnit U = st.units[R.unit_off + h * R.n_ub + b / bpu];
-    const int lr = (b % bpu) * G;
-    for (int p = 0; p < U.n_slots; ++p) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const int64_t pr = (int64_t)(U.first_slot + p) * kUnitRows + lr + g;
-            float v[E];
-            const float* op = st.o_part + pr * D + lane * E;
-            if constexpr (E == 4) {
-                const float4 v4 = *reinterpret_cast<const float4*>(op);
-                v[0] = v4.x; v[1] = v4.y; v[2] = v4.z; v[3] = v4.w;
-            } else {
-#pragma unroll
-                for (int e = 0; e < E; ++e) v[e] = op[e];
-            }
-            mix[g].add(st.lse_part[pr], v);
-        }
-    }
-    // beam part: the t BeamKV tokens on the beam's path
-    const int32_t* path = st.path + ((int64_t)(t - 1) * st.rows + row) * L;
-    for (int j = 0; j < t; ++j) {
-        const int slot = path[j];
-        const int64_t kv = (((int64_t)layer * (L - 1) + j) * st.rows + R.row_off + slot) * Hkv + h;
-        const uint16_t* kp = st.beam_k + kv * D + lane * E;
-        const uint16_t* vp = st.beam_v + kv * D + lane * E;
-        float kf[E], vf[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) { kf[e] = bf16_to_f(kp[e]); vf[e] = bf16_to_f(vp[e]); }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float d = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) d = fmaf(qv[g][e], kf[e], d);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            mix[g].add(d * scale, vf);
-        }
-    }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const float inv = 1.f / mix[g].den;
+        // beam scores
+        float sj[TMAX];
+        float M = -CUDART_INF_F;
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(mix[g].acc[e] * inv, mix[g].acc[e + 1] * inv);
-            *reinterpret_cast<__nv_bfloat162*>(o + g * D + e) = h2;
+        for (int j = 0; j < TMAX; ++j) {
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) d = fmaf(qv[g][e], kf[j][e], d);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+            sj[j] = (j < t) ? d * scale : -CUDART_INF_F;
+            M = fmaxf(M, sj[j]);
         }
+#pragma unroll
+        for (int p = 0; p < kPieces; ++p) M = fmaxf(M, plse[p][g]);
+        for (int p = kPieces; p < n_slots; ++p)
+            M = fmaxf(M, __ldg(st.lse_part + (int64_t)(first + p) * kUnitRows + lr + g));
+        float acc[E], den = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int p = 0; p < kPieces; ++p) {
+            const float w = __expf(plse[p][g] - M);  // 0 for absent pieces
+            den += w;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, pv[p][g][e], acc[e]);
+        }
+        for (int p = kPieces; p < n_slots; ++p) {  // rare: units cut into more than kPieces
+            const int64_t pr = (int64_t)(first + p) * kUnitRows + lr + g;
+            const float w = __expf(__ldg(st.lse_part + pr) - M);
+            den += w;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, __ldg(st.o_part + pr * D + lane * E + e), acc[e]);
+        }
+#pragma unroll
+        for (int j = 0; j < TMAX; ++j) {
+            const float w = __expf(sj[j] - M);  // 0 beyond level t
+            den += w;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, vf[j][e], acc[e]);
+        }
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int e = 0; e < E; e += 2)
+            *reinterpret_cast<__nv_bfloat162*>(o + g * D + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
     }
 }
 
-template <int D>
-cudaError_t launch_beam_attn_d(const GrState& st, int t, int layer, const uint16_t* q, uint16_t* out,
+template <int D, int TMAX>
+cudaError_t launch_beam_attn_t(const GrState& st, int t, int layer, const uint16_t* q, uint16_t* out,
                                cudaStream_t s, int blocks, float scale) {
     switch (st.n_q_heads / st.n_kv_heads) {
-        case 1: k_beam_attn<D, 1><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        case 2: k_beam_attn<D, 2><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        case 4: k_beam_attn<D, 4><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        case 8: k_beam_attn<D, 8><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        case 16: k_beam_attn<D, 16><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
+        case 1: k_beam_attn<D, 1, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
+        case 2: k_beam_attn<D, 2, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
+        case 4: k_beam_attn<D, 4, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
+        case 8: k_beam_attn<D, 8, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
+        case 16: k_beam_attn<D, 16, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+// BeamKV depth buckets keep the per-level registers small for the usual t = 1, 2
+template <int D>
+cudaError_t launch_beam_attn_d(const GrState& st, int t, int layer, const uint16_t* q, uint16_t* out,
+                               cudaStream_t s, int blocks, float scale) {
+    if (t <= 2) return launch_beam_attn_t<D, 2>(st, t, layer, q, out, s, blocks, scale);
+    if (t <= 4) return launch_beam_attn_t<D, 4>(st, t, layer, q, out, s, blocks, scale);
+    return launch_beam_attn_t<D, kMaxLevels>(st, t, layer, q, out, s, blocks, scale);
 }
 
 }  // namespace
