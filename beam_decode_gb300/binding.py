@@ -26,15 +26,14 @@ GR_ERR_TIMEOUT = -6
 GR_ERR_DEVICE = -7
 GR_NOALLOC_MAX_CANDIDATES = 256 * 1024
 
-KERNEL_CTX_ATTN = 0
-KERNEL_BEAM_ATTN = 1
-KERNEL_LOGSOFTMAX = 2
-KERNEL_TOPK = 3
-KERNEL_ADVANCE = 4
-KERNEL_RESULTS = 5
-KERNEL_INIT = 6
-KERNEL_KINDS = 7
-KERNEL_NAMES = ["ctx_attn", "beam_attn", "logsoftmax_gather", "topk_select", "advance", "results", "init"]
+KERNEL_ATTN = 0
+KERNEL_LOGSOFTMAX = 1
+KERNEL_TOPK = 2
+KERNEL_ADVANCE = 3
+KERNEL_RESULTS = 4
+KERNEL_INIT = 5
+KERNEL_KINDS = 6
+KERNEL_NAMES = ["attn", "logsoftmax_gather", "topk_select", "advance", "results", "init"]
 
 # exported symbols of include/grbeam.h
 SYMBOLS = [

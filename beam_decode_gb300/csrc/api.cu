@@ -278,7 +278,8 @@ struct Schedule {
 
 struct WsLayout {
     size_t req, row_req, n_beams, parent, token, node, score, path, cand, sel_parent, sel_code, sel_key, n_sel,
-        status, tmaps, jobs, cta_jobs, units, combine_meta, tables_end, o_part, lse_part, res_codes, res_items, res_scores, total;
+        status, tmaps, jobs, cta_jobs, units, tables_end, o_part, lse_part, piece_flag, res_codes, res_items, res_scores,
+        total;
 };
 
 gr_status check_config(const gr_config* c, const gr_request* reqs, int n) {
@@ -394,7 +395,6 @@ WsLayout ws_layout(const gr_config* c, int n, int rows, const Schedule& s) {
     w.jobs = take(sizeof(GrAttnJob) * s.jobs.size());
     w.cta_jobs = take(sizeof(int2) * s.cta_jobs.size());
     w.units = take(sizeof(GrAttnUnit) * s.units.size());
-    w.combine_meta = take(sizeof(int4) * rows * c->n_kv_heads);
     w.tables_end = align_up(o, 256);
     // device state
     w.n_beams = take(4ull * n * (L + 1));
@@ -411,6 +411,7 @@ WsLayout ws_layout(const gr_config* c, int n, int rows, const Schedule& s) {
     w.status = take(16);
     w.o_part = take(4ull * s.jobs.size() * kUnitRows * c->head_dim);
     w.lse_part = take(4ull * s.jobs.size() * kUnitRows);
+    w.piece_flag = take(4ull * s.jobs.size() * kUnitRows);
     w.res_codes = take(4ull * rows * L);
     w.res_items = take(8ull * rows);
     w.res_scores = take(4ull * rows);
@@ -445,6 +446,7 @@ struct gr_beam {
     std::vector<Ev> events[GR_KERNEL_KINDS];
     std::vector<Ev> event_pool;
     int64_t wait_limit_ns = 2000000000ll;
+    uint32_t attn_epoch = 0;
 
     ~gr_beam() {
         for (int k = 0; k < GR_KERNEL_KINDS; ++k)
@@ -581,7 +583,7 @@ extern "C" gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs
         st.jobs = reinterpret_cast<GrAttnJob*>(ws + w.jobs);
         st.cta_jobs = reinterpret_cast<int2*>(ws + w.cta_jobs);
         st.units = reinterpret_cast<GrAttnUnit*>(ws + w.units);
-        st.combine_meta = reinterpret_cast<int4*>(ws + w.combine_meta);
+        st.piece_flag = reinterpret_cast<uint32_t*>(ws + w.piece_flag);
         st.n_units = (int)h->sched.units.size();
         st.n_jobs = (int)h->sched.jobs.size();
         st.n_cta = (int)h->sched.cta_jobs.size();
@@ -633,20 +635,8 @@ extern "C" gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs
         memcpy(img.data() + w.jobs, h->sched.jobs.data(), sizeof(GrAttnJob) * h->sched.jobs.size());
         memcpy(img.data() + w.cta_jobs, h->sched.cta_jobs.data(), sizeof(int2) * h->sched.cta_jobs.size());
         memcpy(img.data() + w.units, h->sched.units.data(), sizeof(GrAttnUnit) * h->sched.units.size());
-        // combine table: for (row, KV head) the context pieces holding that row's partials
-        {
-            int4* cm = reinterpret_cast<int4*>(img.data() + w.combine_meta);
-            const int G = cfg->n_q_heads / cfg->n_kv_heads;
-            const int bpu = kUnitRows / G;
-            for (int r = 0; r < n_requests; ++r)
-                for (int b = 0; b < reqs[r].beam_width; ++b)
-                    for (int hh = 0; hh < cfg->n_kv_heads; ++hh) {
-                        const GrAttnUnit& u = h->sched.units[unit_off[r] + hh * n_ub[r] + b / bpu];
-                        cm[(size_t)(h->row_off[r] + b) * cfg->n_kv_heads + hh] =
-                            make_int4(u.first_slot, (u.n_slots << 16) | ((b % bpu) * G), b, reqs[r].beam_width);
-                    }
-        }
         cudaError_t e = cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaMemsetAsync(st.piece_flag, 0, 4ull * h->sched.jobs.size() * kUnitRows, cs);
         if (e == cudaSuccess) e = launch_init_state(st, cs);
         if (e == cudaSuccess) e = cudaStreamSynchronize(cs);  // img is released on return
         if (e != cudaSuccess) {
@@ -711,12 +701,11 @@ extern "C" gr_status gr_decode_attn(gr_beam* h, int layer, const void* q, void* 
     if (s != GR_OK) return s;
     cudaStream_t cs = (cudaStream_t)stream;
     const int64_t lim = h->wait_limit_ns;
-    if ((s = run_kernel(h, GR_KERNEL_CTX_ATTN, cs, [&] { return launch_ctx_attn(h->st, qmap, layer, lim, cs); })) !=
-        GR_OK)
-        return s;
     const int t = h->step;
-    if ((s = run_kernel(h, GR_KERNEL_BEAM_ATTN, cs, [&] {
-             return launch_beam_attn(h->st, t, layer, static_cast<const uint16_t*>(q), static_cast<uint16_t*>(out), cs);
+    const uint32_t epoch = ++h->attn_epoch;  // tags the pieces this launch publishes
+    if ((s = run_kernel(h, GR_KERNEL_ATTN, cs, [&] {
+             return launch_ctx_attn(h->st, qmap, layer, t, static_cast<const uint16_t*>(q),
+                                    static_cast<uint16_t*>(out), epoch, lim, cs);
          })) != GR_OK)
         return s;
     h->attn_done[layer] = 1;

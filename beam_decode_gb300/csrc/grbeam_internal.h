@@ -93,9 +93,9 @@ struct GrState {
     int2* cta_jobs;     // [n_cta] job range of each CTA
     GrAttnUnit* units;  // [n_units]
     int n_units, n_jobs, n_cta;
-    float* o_part;      // [n_jobs][kUnitRows][D]
+    float* o_part;      // [n_jobs][kUnitRows][D] pieces of split units (later key ranges)
     float* lse_part;    // [n_jobs][kUnitRows]
-    int4* combine_meta; // [rows][Hkv]: first slot, (slots << 16 | row within the unit), beam, W_r
+    uint32_t* piece_flag; // [n_jobs][kUnitRows] launch epoch of the last published piece row
     const uint16_t* beam_k; // bf16 [NL][L-1][rows][Hkv][D]
     const uint16_t* beam_v;
 
@@ -116,9 +116,7 @@ cudaError_t launch_results(const GrState& st, cudaStream_t s);
 
 // ---- launchers (k_attn.cu) ----
 cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes);
-cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer,
-                            int64_t wait_limit_ns, cudaStream_t s);
-cudaError_t launch_beam_attn(const GrState& st, int t, int layer, const uint16_t* q, uint16_t* out,
-                             cudaStream_t s);
+cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, int t, const uint16_t* q,
+                            uint16_t* out, uint32_t epoch, int64_t wait_limit_ns, cudaStream_t s);
 
 }  // namespace grb

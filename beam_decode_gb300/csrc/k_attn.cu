@@ -23,17 +23,22 @@
 //              rescale of O (only when the running max grows by more than
 //              2^8), P written back to TMEM as bf16 in place of S.
 //   The two query tiles ping-pong: while one warpgroup exponentiates, the
-//   tensor core runs the other tile's MMAs.  Each job writes its normalised
-//   partial O (fp32) and log-sum-exp to a slot of the workspace.
+//   tensor core runs the other tile's MMAs.
 // Units of one (request, KV head) are scheduled on neighbouring CTAs so the
 // second read of a K/V tile is served by L2; each context byte comes from HBM
 // once per request.
 //
-// k_beam_attn: one warp per (row, KV head).  The t BeamKV keys of the beam are
-// found through its ancestry row (levels 0..t-1) and read with vector loads;
-// scores are warp reductions; the context partials and the beam part are
-// merged with a log-sum-exp combine and written as bf16.
-//
+// Epilogue: a unit whose key tiles were cut over several CTAs is finished by
+// its first key range, which by construction of the schedule is the last job
+// of its CTA; the later ranges run at the start of the next CTAs and publish
+// their normalised fp32 piece, its log-sum-exp and a per-row ready flag
+// tagged with the launch epoch.  The first range merges them with its own O
+// (still in registers) and with the beam part -- the t BeamKV keys found
+// through the beam's ancestry row (levels 0..t-1) -- by a log-sum-exp
+// combine, and writes the bf16 output row.  Rows of dead beams are written
+// as zeros.  The launch is cooperative, so every CTA a merger waits for is
+// resident.
+
 // Every wait inside k_ctx_attn is bounded: past the limit the kernel flags
 // GR_ERR_TIMEOUT, drains the copies and MMAs it issued, frees TMEM and returns.
 #include <cuda.h>
@@ -281,6 +286,26 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
+// one thread waits for a flag written by another CTA of the same (cooperative) launch
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t value, const Waiter w) {
+    const volatile uint32_t* f = reinterpret_cast<const volatile uint32_t*>(flag);
+    if (*f == value) return true;
+    const uint64_t t0 = global_timer();
+    uint32_t spins = 0;
+    while (*f != value) {
+        if (w.limit < 0 || ((++spins) & 31) == 0) {
+            if (*w.abort) return false;
+            if (w.limit < 0 || (int64_t)(global_timer() - t0) > w.limit) {
+                *w.abort = 1;
+                atomicOr(w.status, kStatusTimeout);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // shared-memory plan
 // ---------------------------------------------------------------------------
@@ -312,8 +337,8 @@ constexpr int kAttnThreads = 384;
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, float scale_log2, float scale,
-           int64_t wait_limit_ns) {
+k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int t, const uint16_t* __restrict__ q,
+           uint16_t* __restrict__ out, uint32_t epoch, float scale_log2, float scale, int64_t wait_limit_ns) {
     using P = Plan<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -523,6 +548,44 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
             if (i >= U.nqt) continue;
             const int ctx_len = st.req[U.req].ctx_len;
             const int n = J.t1 - J.t0;
+            const bool merger = (J.slot == U.first_slot);
+            // this row's beam and query head; the beam part of its scores is computed now,
+            // while the first S tile is still being produced
+            const GrReqDev& R = st.req[U.req];
+            const int b = U.beam0 + i * (kTileRows / G) + row_t / G;
+            const int g = row_t % G;
+            const bool row_ok = b < R.width;
+            const bool live = row_ok && t < R.n_levels && b < st.n_beams[U.req * (st.n_levels + 1) + t];
+            const int64_t orow_idx = (int64_t)(R.row_off + b) * st.n_q_heads + U.head * G + g;
+            const int L = st.n_levels;
+            float sj[kMaxLevels];
+            int64_t kvj[kMaxLevels];
+            if (merger && live) {
+                const int32_t* path = st.path + ((int64_t)(t - 1) * st.rows + R.row_off + b) * L;
+                const uint4* qrow = reinterpret_cast<const uint4*>(q + orow_idx * D);
+                for (int j = 0; j < t; ++j) {
+                    kvj[j] = (((int64_t)layer * (L - 1) + j) * st.rows + R.row_off + path[j]) * st.n_kv_heads + U.head;
+                    const uint4* krow = reinterpret_cast<const uint4*>(st.beam_k + kvj[j] * D);
+                    float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                    for (int half = 0; half < D / 64; ++half) {
+                        uint4 qa[8], ka[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) { qa[e] = __ldg(qrow + 8 * half + e); ka[e] = __ldg(krow + 8 * half + e); }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const uint32_t qw[4] = {qa[e].x, qa[e].y, qa[e].z, qa[e].w};
+                            const uint32_t kw[4] = {ka[e].x, ka[e].y, ka[e].z, ka[e].w};
+#pragma unroll
+                            for (int h2 = 0; h2 < 4; ++h2) {
+                                d0 = fmaf(__uint_as_float(qw[h2] << 16), __uint_as_float(kw[h2] << 16), d0);
+                                d1 = fmaf(__uint_as_float(qw[h2] & 0xFFFF0000u), __uint_as_float(kw[h2] & 0xFFFF0000u), d1);
+                            }
+                        }
+                    }
+                    sj[j] = (d0 + d1) * scale;
+                }
+            }
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int jj = 0; jj < n; ++jj) {
                 if (!(ok = wait_warp(bar(B_S_FULL + i), tiles & 1, wt))) break;
@@ -593,203 +656,150 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, floa
                 ++tiles;
             }
             if (!ok) break;
-            // epilogue: normalised partial O and its log-sum-exp
+            // epilogue
             if (!(ok = wait_warp(bar(B_O_FULL + i), jobs & 1, wt))) break;
             tc_fence_after();
+            const float lse_own = m_used * scale + logf(l);
             const float inv_l = 1.f / l;
             const int prow = i * kTileRows + row_t;
-            float* orow = st.o_part + ((int64_t)J.slot * kUnitRows + prow) * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(tmem + lane_base + P::o_col(i) + 32 * c, ov);
-                float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
+            uint32_t ov[D];  // this piece's unnormalised O row
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv_l, __uint_as_float(ov[4 * e + 1]) * inv_l,
-                                         __uint_as_float(ov[4 * e + 2]) * inv_l, __uint_as_float(ov[4 * e + 3]) * inv_l);
-            }
-            st.lse_part[(int64_t)J.slot * kUnitRows + prow] = m_used * scale + logf(l);
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_base + P::o_col(i) + 32 * c, ov + 32 * c);
             tc_fence_before();
-            mbar_arrive(bar(B_O_EMPTY + i));
+            mbar_arrive(bar(B_O_EMPTY + i));  // TMEM O is free for the next job
             ++jobs;
+            const int piece = J.slot - U.first_slot;
+            if (piece != 0) {
+                // a later key range of a split unit: publish the normalised piece and its
+                // log-sum-exp, then this row's ready flag (tagged with the launch epoch)
+                float* orow = st.o_part + ((int64_t)J.slot * kUnitRows + prow) * D;
+#pragma unroll
+                for (int e = 0; e < D / 4; ++e)
+                    __stcg(reinterpret_cast<float4*>(orow) + e,
+                           make_float4(__uint_as_float(ov[4 * e]) * inv_l, __uint_as_float(ov[4 * e + 1]) * inv_l,
+                                       __uint_as_float(ov[4 * e + 2]) * inv_l, __uint_as_float(ov[4 * e + 3]) * inv_l));
+                __stcg(st.lse_part + (int64_t)J.slot * kUnitRows + prow, lse_own);
+                __threadfence();
+                *reinterpret_cast<volatile uint32_t*>(st.piece_flag + (int64_t)J.slot * kUnitRows + prow) = epoch;
+                continue;
+            }
+            // the first key range merges: the other pieces of the unit (finished earlier,
+            // at the start of their CTAs' ranges) and the beam's BeamKV tokens
+            if (!row_ok) continue;  // row of the tile beyond this request
+            uint4* dst = reinterpret_cast<uint4*>(out + orow_idx * D);
+            if (!live) {
+#pragma unroll
+                for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);  // dead beam
+                continue;
+            }
+            // wait (bounded) for the other pieces of this row
+            const int n_other = U.n_slots - 1;
+            const float* lse_col = st.lse_part + (int64_t)U.first_slot * kUnitRows + prow;
+            bool have = true;
+            for (int pp = 1; pp <= n_other && have; ++pp)
+                have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, epoch, wt);
+            if (!have) { ok = false; break; }
+            __threadfence();
+            constexpr int kRegPieces = 2;  // pieces merged from registers; more are streamed
+            float lse_o[kRegPieces];
+            float M = lse_own;
+#pragma unroll
+            for (int pp = 0; pp < kRegPieces; ++pp) {
+                lse_o[pp] = (pp < n_other) ? __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) : -CUDART_INF_F;
+                M = fmaxf(M, lse_o[pp]);
+            }
+            for (int pp = kRegPieces; pp < n_other; ++pp) M = fmaxf(M, __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows));
+            for (int j = 0; j < t; ++j) M = fmaxf(M, sj[j]);
+            const float w_own = __expf(lse_own - M);
+            float den = w_own;
+            float w_o[kRegPieces];
+#pragma unroll
+            for (int pp = 0; pp < kRegPieces; ++pp) { w_o[pp] = __expf(lse_o[pp] - M); den += w_o[pp]; }
+            for (int pp = kRegPieces; pp < n_other; ++pp) den += __expf(__ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) - M);
+            float w_j[kMaxLevels];
+            for (int j = 0; j < t; ++j) { w_j[j] = __expf(sj[j] - M); den += w_j[j]; }
+            const float inv_den = 1.f / den;
+            const float c_own = w_own * inv_l * inv_den;
+#pragma unroll
+            for (int pp = 0; pp < kRegPieces; ++pp) w_o[pp] *= inv_den;
+            for (int j = 0; j < t; ++j) w_j[j] *= inv_den;
+            // 32 output columns at a time: every load of a quarter is issued before use
+#pragma unroll
+            for (int qd = 0; qd < D / 32; ++qd) {
+                float a[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) a[u] = __uint_as_float(ov[32 * qd + u]) * c_own;
+                float4 pv[kRegPieces][8];
+#pragma unroll
+                for (int pp = 0; pp < kRegPieces; ++pp) {
+                    if (pp < n_other) {
+                        const float4* op = reinterpret_cast<const float4*>(
+                            st.o_part + ((int64_t)(U.first_slot + pp + 1) * kUnitRows + prow) * D + 32 * qd);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) pv[pp][e] = __ldcg(op + e);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) pv[pp][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                uint4 vv[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (j < t) {
+                        const uint4* vp = reinterpret_cast<const uint4*>(st.beam_v + kvj[j] * D + 32 * qd);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) vv[j][e] = __ldg(vp + e);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) vv[j][e] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int pp = 0; pp < kRegPieces; ++pp)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        a[4 * e + 0] = fmaf(w_o[pp], pv[pp][e].x, a[4 * e + 0]);
+                        a[4 * e + 1] = fmaf(w_o[pp], pv[pp][e].y, a[4 * e + 1]);
+                        a[4 * e + 2] = fmaf(w_o[pp], pv[pp][e].z, a[4 * e + 2]);
+                        a[4 * e + 3] = fmaf(w_o[pp], pv[pp][e].w, a[4 * e + 3]);
+                    }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float wj = (j < t) ? w_j[j] : 0.f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t vw[4] = {vv[j][e].x, vv[j][e].y, vv[j][e].z, vv[j][e].w};
+#pragma unroll
+                        for (int h2 = 0; h2 < 4; ++h2) {
+                            a[8 * e + 2 * h2] = fmaf(wj, __uint_as_float(vw[h2] << 16), a[8 * e + 2 * h2]);
+                            a[8 * e + 2 * h2 + 1] = fmaf(wj, __uint_as_float(vw[h2] & 0xFFFF0000u), a[8 * e + 2 * h2 + 1]);
+                        }
+                    }
+                }
+                // rare: more pieces or deeper BeamKV than the register path holds
+                for (int pp = kRegPieces; pp < n_other; ++pp) {
+                    const int64_t pr = (int64_t)(U.first_slot + pp + 1) * kUnitRows + prow;
+                    const float w = __expf(__ldcg(st.lse_part + pr) - M) * inv_den;
+                    const float* op = st.o_part + pr * D + 32 * qd;
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) a[u] = fmaf(w, __ldcg(op + u), a[u]);
+                }
+                for (int j = 2; j < t; ++j) {
+                    const uint16_t* vp = st.beam_v + kvj[j] * D + 32 * qd;
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) a[u] = fmaf(w_j[j], __uint_as_float((uint32_t)__ldg(vp + u) << 16), a[u]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[4 * qd + e] = make_uint4(pack_bf16x2(a[8 * e], a[8 * e + 1]), pack_bf16x2(a[8 * e + 2], a[8 * e + 3]),
+                                                 pack_bf16x2(a[8 * e + 4], a[8 * e + 5]),
+                                                 pack_bf16x2(a[8 * e + 6], a[8 * e + 7]));
+            }
         }
     }
     tc_fence_before();
     named_bar_sync(1);
     named_bar_sync(2);
-}
-
-// ---------------------------------------------------------------------------
-// K2: BeamKV part + log-sum-exp combine with the context partials
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float bf16_to_f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
-
-template <int D, int G, int TMAX>
-__global__ void __launch_bounds__(256) k_beam_attn(GrState st, int t, int layer, const uint16_t* __restrict__ q,
-                                                   uint16_t* __restrict__ out, float scale) {
-    constexpr int E = D / 32;  // elements per lane
-    constexpr int kPieces = 3;  // context pieces held in registers (more are streamed)
-    const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    const int Hkv = st.n_kv_heads, Hq = st.n_q_heads, L = st.n_levels;
-    if (gw >= st.rows * Hkv) return;
-    const int row = gw / Hkv, h = gw % Hkv;
-    // round 1: everything that depends only on (row, head)
-    const int4 meta = st.combine_meta[gw];  // first slot, slots << 16 | local row, beam, request width
-    const int r = st.row_req[row];
-    const uint16_t* qp = q + ((int64_t)row * Hq + h * G) * D + lane * E;
-    uint16_t* o = out + ((int64_t)row * Hq + h * G) * D + lane * E;
-    float qv[G][E];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if constexpr (E == 4) {
-            const uint2 u = __ldg(reinterpret_cast<const uint2*>(qp + g * D));
-            qv[g][0] = __uint_as_float(u.x << 16); qv[g][1] = __uint_as_float(u.x & 0xFFFF0000u);
-            qv[g][2] = __uint_as_float(u.y << 16); qv[g][3] = __uint_as_float(u.y & 0xFFFF0000u);
-        } else {
-            const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(qp + g * D));
-            qv[g][0] = __uint_as_float(u << 16); qv[g][1] = __uint_as_float(u & 0xFFFF0000u);
-        }
-    }
-    // ancestry row: only written for live beams, so every slot is clamped into the
-    // request's rows before it forms an address (a dead row's result is discarded)
-    const int32_t* path = st.path + ((int64_t)(t - 1) * st.rows + row) * L;
-    const int width = meta.w;
-    int slot[TMAX];
-#pragma unroll
-    for (int j = 0; j < TMAX; ++j) {
-        const int v = (j < t) ? __ldg(path + j) : 0;
-        slot[j] = ((unsigned)v < (unsigned)width) ? v : 0;
-    }
-    // round 2: live width, context pieces, BeamKV rows
-    const int n_live = st.n_beams[r * (L + 1) + t];
-    const int b = meta.z, lr = meta.y & 0xFFFF, first = meta.x, n_slots = meta.y >> 16;
-    float plse[kPieces][G], pv[kPieces][G][E];
-#pragma unroll
-    for (int p = 0; p < kPieces; ++p) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            if (p < n_slots) {
-                const int64_t pr = (int64_t)(first + p) * kUnitRows + lr + g;
-                plse[p][g] = __ldg(st.lse_part + pr);
-                const float* op = st.o_part + pr * D + lane * E;
-                if constexpr (E == 4) {
-                    const float4 v4 = __ldg(reinterpret_cast<const float4*>(op));
-                    pv[p][g][0] = v4.x; pv[p][g][1] = v4.y; pv[p][g][2] = v4.z; pv[p][g][3] = v4.w;
-                } else {
-                    const float2 v2 = __ldg(reinterpret_cast<const float2*>(op));
-                    pv[p][g][0] = v2.x; pv[p][g][1] = v2.y;
-                }
-            } else {
-                plse[p][g] = -CUDART_INF_F;
-#pragma unroll
-                for (int e = 0; e < E; ++e) pv[p][g][e] = 0.f;
-            }
-        }
-    }
-    float kf[TMAX][E], vf[TMAX][E];
-#pragma unroll
-    for (int j = 0; j < TMAX; ++j) {
-        if (j < t) {
-            const int64_t kv = (((int64_t)layer * (L - 1) + j) * st.rows + (row - b) + slot[j]) * Hkv + h;
-            const uint16_t* kp = st.beam_k + kv * D + lane * E;
-            const uint16_t* vp = st.beam_v + kv * D + lane * E;
-            if constexpr (E == 4) {
-                const uint2 ku = __ldg(reinterpret_cast<const uint2*>(kp)), vu = __ldg(reinterpret_cast<const uint2*>(vp));
-                kf[j][0] = __uint_as_float(ku.x << 16); kf[j][1] = __uint_as_float(ku.x & 0xFFFF0000u);
-                kf[j][2] = __uint_as_float(ku.y << 16); kf[j][3] = __uint_as_float(ku.y & 0xFFFF0000u);
-                vf[j][0] = __uint_as_float(vu.x << 16); vf[j][1] = __uint_as_float(vu.x & 0xFFFF0000u);
-                vf[j][2] = __uint_as_float(vu.y << 16); vf[j][3] = __uint_as_float(vu.y & 0xFFFF0000u);
-            } else {
-                const uint32_t ku = __ldg(reinterpret_cast<const uint32_t*>(kp));
-                const uint32_t vu = __ldg(reinterpret_cast<const uint32_t*>(vp));
-                kf[j][0] = __uint_as_float(ku << 16); kf[j][1] = __uint_as_float(ku & 0xFFFF0000u);
-                vf[j][0] = __uint_as_float(vu << 16); vf[j][1] = __uint_as_float(vu & 0xFFFF0000u);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < E; ++e) { kf[j][e] = 0.f; vf[j][e] = 0.f; }
-        }
-    }
-    if (t >= st.req[r].n_levels || b >= n_live) {
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(o + g * D + e) = 0u;
-        return;
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        // beam scores
-        float sj[TMAX];
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int j = 0; j < TMAX; ++j) {
-            float d = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) d = fmaf(qv[g][e], kf[j][e], d);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            sj[j] = (j < t) ? d * scale : -CUDART_INF_F;
-            M = fmaxf(M, sj[j]);
-        }
-#pragma unroll
-        for (int p = 0; p < kPieces; ++p) M = fmaxf(M, plse[p][g]);
-        for (int p = kPieces; p < n_slots; ++p)
-            M = fmaxf(M, __ldg(st.lse_part + (int64_t)(first + p) * kUnitRows + lr + g));
-        float acc[E], den = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = 0.f;
-#pragma unroll
-        for (int p = 0; p < kPieces; ++p) {
-            const float w = __expf(plse[p][g] - M);  // 0 for absent pieces
-            den += w;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, pv[p][g][e], acc[e]);
-        }
-        for (int p = kPieces; p < n_slots; ++p) {  // rare: units cut into more than kPieces
-            const int64_t pr = (int64_t)(first + p) * kUnitRows + lr + g;
-            const float w = __expf(__ldg(st.lse_part + pr) - M);
-            den += w;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, __ldg(st.o_part + pr * D + lane * E + e), acc[e]);
-        }
-#pragma unroll
-        for (int j = 0; j < TMAX; ++j) {
-            const float w = __expf(sj[j] - M);  // 0 beyond level t
-            den += w;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, vf[j][e], acc[e]);
-        }
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int e = 0; e < E; e += 2)
-            *reinterpret_cast<__nv_bfloat162*>(o + g * D + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-    }
-}
-
-template <int D, int TMAX>
-cudaError_t launch_beam_attn_t(const GrState& st, int t, int layer, const uint16_t* q, uint16_t* out,
-                               cudaStream_t s, int blocks, float scale) {
-    switch (st.n_q_heads / st.n_kv_heads) {
-        case 1: k_beam_attn<D, 1, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        case 2: k_beam_attn<D, 2, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        case 4: k_beam_attn<D, 4, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        case 8: k_beam_attn<D, 8, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        case 16: k_beam_attn<D, 16, TMAX><<<blocks, 256, 0, s>>>(st, t, layer, q, out, scale); break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
-}
-
-// BeamKV depth buckets keep the per-level registers small for the usual t = 1, 2
-template <int D>
-cudaError_t launch_beam_attn_d(const GrState& st, int t, int layer, const uint16_t* q, uint16_t* out,
-                               cudaStream_t s, int blocks, float scale) {
-    if (t <= 2) return launch_beam_attn_t<D, 2>(st, t, layer, q, out, s, blocks, scale);
-    if (t <= 4) return launch_beam_attn_t<D, 4>(st, t, layer, q, out, s, blocks, scale);
-    return launch_beam_attn_t<D, kMaxLevels>(st, t, layer, q, out, s, blocks, scale);
 }
 
 }  // namespace
@@ -801,43 +811,41 @@ cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes) {
     return cudaSuccess;
 }
 
-cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, int64_t wait_limit_ns,
-                            cudaStream_t s) {
-    const float scale = 1.f / sqrtf((float)st.head_dim);
-    const float scale_log2 = scale * 1.4426950408889634f;
-    if (st.head_dim == 128) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(k_ctx_attn<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 Plan<128>::kBytes);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        k_ctx_attn<128><<<st.n_cta, kAttnThreads, Plan<128>::kBytes, s>>>(qmap, st, layer, scale_log2, scale,
-                                                                           wait_limit_ns);
-    } else if (st.head_dim == 64) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(k_ctx_attn<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 Plan<64>::kBytes);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        k_ctx_attn<64><<<st.n_cta, kAttnThreads, Plan<64>::kBytes, s>>>(qmap, st, layer, scale_log2, scale,
-                                                                         wait_limit_ns);
-    } else {
-        return cudaErrorInvalidValue;
+template <int D>
+cudaError_t launch_ctx_attn_d(const GrState& st, const CUtensorMap& qmap, int layer, int t, const uint16_t* q,
+                              uint16_t* out, uint32_t epoch, float scale_log2, float scale, int64_t wait_limit_ns,
+                              cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_ctx_attn<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Plan<D>::kBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
     }
-    return cudaGetLastError();
+    // cooperative: every CTA is resident at once, so a merging CTA may wait for the
+    // flags of the pieces other CTAs publish
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(st.n_cta);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = Plan<D>::kBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_ctx_attn<D>, qmap, st, layer, t, q, out, epoch, scale_log2, scale,
+                              wait_limit_ns);
 }
 
-cudaError_t launch_beam_attn(const GrState& st, int t, int layer, const uint16_t* q, uint16_t* out,
-                             cudaStream_t s) {
+cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, int t, const uint16_t* q,
+                            uint16_t* out, uint32_t epoch, int64_t wait_limit_ns, cudaStream_t s) {
     const float scale = 1.f / sqrtf((float)st.head_dim);
-    const int64_t warps = (int64_t)st.rows * st.n_kv_heads;
-    const int blocks = (int)((warps * 32 + 255) / 256);
-    if (st.head_dim == 128) return launch_beam_attn_d<128>(st, t, layer, q, out, s, blocks, scale);
-    if (st.head_dim == 64) return launch_beam_attn_d<64>(st, t, layer, q, out, s, blocks, scale);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    if (st.head_dim == 128)
+        return launch_ctx_attn_d<128>(st, qmap, layer, t, q, out, epoch, scale_log2, scale, wait_limit_ns, s);
+    if (st.head_dim == 64)
+        return launch_ctx_attn_d<64>(st, qmap, layer, t, q, out, epoch, scale_log2, scale, wait_limit_ns, s);
     return cudaErrorInvalidValue;
 }
 

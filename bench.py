@@ -291,7 +291,7 @@ def run_gpu(args, w):
 
     # roofline of the dominant kernel (shared-context attention)
     pk = _peaks()
-    n_att, t_att = stats["ctx_attn"]
+    n_att, t_att = stats["attn"]
     att_ms = t_att / max(n_att, 1)
     flops_launch = batch.attn_flops() / w.n_layers
     achieved = flops_launch / (att_ms * 1e-3) / 1e12
@@ -306,14 +306,11 @@ def run_gpu(args, w):
     per_kernel = {k: {"launches": n, "ms_per_launch": (t / n if n else 0.0), "ms_per_step": t / args.steps}
                   for k, (n, t) in stats.items() if n}
     hbm = {}
-    for name in ("beam_attn", "logsoftmax_gather"):
-        n, t = stats[name]
-        if n:
-            if name == "logsoftmax_gather":
-                byts = batch.rows * w.vocab * 4.0
-            else:
-                byts = batch.rows * w.n_q_heads * w.head_dim * 2 * 2 + batch.rows * w.n_kv_heads * w.head_dim * 2 * 2
-            hbm[name] = {"GB_s": byts / (t / n * 1e-3) / 1e9, "frac": byts / (t / n * 1e-3) / 1e9 / pk["hbm"]}
+    n, t = stats["logsoftmax_gather"]
+    if n:
+        byts = batch.rows * w.vocab * 4.0
+        hbm["logsoftmax_gather"] = {"GB_s": byts / (t / n * 1e-3) / 1e9,
+                                    "frac": byts / (t / n * 1e-3) / 1e9 / pk["hbm"]}
 
     if rank == 0:
         cpu_s, sample = oracle_step_seconds(w, budget_s=12.0) if not args.no_cpu else (float("nan"), "skipped")

@@ -221,14 +221,14 @@ gr_status gr_beam_status(gr_beam* beam, int clear_flag, gr_stream_t stream);
 /* ------------------------------------------------------------------------ */
 
 /* Kernel kinds, for gr_beam_kernel_stats. */
-#define GR_KERNEL_CTX_ATTN    0  /* shared-context attention (tensor cores)        */
-#define GR_KERNEL_BEAM_ATTN   1  /* BeamKV attention + log-sum-exp combine          */
-#define GR_KERNEL_LOGSOFTMAX  2  /* full-vocab log-softmax + level gather + mask    */
-#define GR_KERNEL_TOPK        3  /* cross-beam top-K selection per request          */
-#define GR_KERNEL_ADVANCE     4  /* BeamPath advance                                */
-#define GR_KERNEL_RESULTS     5  /* result gather                                    */
-#define GR_KERNEL_INIT        6  /* state initialisation                             */
-#define GR_KERNEL_KINDS       7
+#define GR_KERNEL_ATTN        0  /* decode attention: shared context on the tensor cores,
+                                    BeamKV part and log-sum-exp combine in its epilogue */
+#define GR_KERNEL_LOGSOFTMAX  1  /* full-vocab log-softmax + level gather + mask    */
+#define GR_KERNEL_TOPK        2  /* cross-beam top-K selection per request          */
+#define GR_KERNEL_ADVANCE     3  /* BeamPath advance                                */
+#define GR_KERNEL_RESULTS     4  /* result gather                                    */
+#define GR_KERNEL_INIT        5  /* state initialisation                             */
+#define GR_KERNEL_KINDS       6
 
 /* enable != 0: bracket every kernel launch with CUDA events on its stream
  * (host-side event objects; no device memory). */
