@@ -93,7 +93,7 @@ struct GrState {
     int2* cta_jobs;     // [n_cta] job range of each CTA
     GrAttnUnit* units;  // [n_units]
     int n_units, n_jobs, n_cta;
-    float* o_part;      // [n_jobs][kUnitRows][D] pieces of split units (later key ranges)
+    float* o_part;      // [n_jobs][D][kUnitRows] pieces of split units (later key ranges), column-major
     float* lse_part;    // [n_jobs][kUnitRows]
     uint32_t* piece_flag; // [n_jobs][kUnitRows] launch epoch of the last published piece row
     const uint16_t* beam_k; // bf16 [NL][L-1][rows][Hkv][D]

@@ -672,12 +672,11 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
             if (piece != 0) {
                 // a later key range of a split unit: publish the normalised piece and its
                 // log-sum-exp, then this row's ready flag (tagged with the launch epoch)
-                float* orow = st.o_part + ((int64_t)J.slot * kUnitRows + prow) * D;
+                // column-major piece [slot][D][256 rows]: a warp stores 32 consecutive rows of
+                // one column per instruction (one 128-byte transaction)
+                float* ocol = st.o_part + (int64_t)J.slot * D * kUnitRows + prow;
 #pragma unroll
-                for (int e = 0; e < D / 4; ++e)
-                    __stcg(reinterpret_cast<float4*>(orow) + e,
-                           make_float4(__uint_as_float(ov[4 * e]) * inv_l, __uint_as_float(ov[4 * e + 1]) * inv_l,
-                                       __uint_as_float(ov[4 * e + 2]) * inv_l, __uint_as_float(ov[4 * e + 3]) * inv_l));
+                for (int c = 0; c < D; ++c) __stcg(ocol + (int64_t)c * kUnitRows, __uint_as_float(ov[c]) * inv_l);
                 __stcg(st.lse_part + (int64_t)J.slot * kUnitRows + prow, lse_own);
                 __threadfence();
                 *reinterpret_cast<volatile uint32_t*>(st.piece_flag + (int64_t)J.slot * kUnitRows + prow) = epoch;
@@ -729,17 +728,16 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
                 float a[32];
 #pragma unroll
                 for (int u = 0; u < 32; ++u) a[u] = __uint_as_float(ov[32 * qd + u]) * c_own;
-                float4 pv[kRegPieces][8];
+                float pv[kRegPieces][32];
 #pragma unroll
                 for (int pp = 0; pp < kRegPieces; ++pp) {
                     if (pp < n_other) {
-                        const float4* op = reinterpret_cast<const float4*>(
-                            st.o_part + ((int64_t)(U.first_slot + pp + 1) * kUnitRows + prow) * D + 32 * qd);
+                        const float* op = st.o_part + ((int64_t)(U.first_slot + pp + 1) * D + 32 * qd) * kUnitRows + prow;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) pv[pp][e] = __ldcg(op + e);
+                        for (int u = 0; u < 32; ++u) pv[pp][u] = __ldcg(op + (int64_t)u * kUnitRows);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) pv[pp][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int u = 0; u < 32; ++u) pv[pp][u] = 0.f;
                     }
                 }
                 uint4 vv[2][4];
@@ -757,12 +755,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
 #pragma unroll
                 for (int pp = 0; pp < kRegPieces; ++pp)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        a[4 * e + 0] = fmaf(w_o[pp], pv[pp][e].x, a[4 * e + 0]);
-                        a[4 * e + 1] = fmaf(w_o[pp], pv[pp][e].y, a[4 * e + 1]);
-                        a[4 * e + 2] = fmaf(w_o[pp], pv[pp][e].z, a[4 * e + 2]);
-                        a[4 * e + 3] = fmaf(w_o[pp], pv[pp][e].w, a[4 * e + 3]);
-                    }
+                    for (int u = 0; u < 32; ++u) a[u] = fmaf(w_o[pp], pv[pp][u], a[u]);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const float wj = (j < t) ? w_j[j] : 0.f;
@@ -778,11 +771,11 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
                 }
                 // rare: more pieces or deeper BeamKV than the register path holds
                 for (int pp = kRegPieces; pp < n_other; ++pp) {
-                    const int64_t pr = (int64_t)(U.first_slot + pp + 1) * kUnitRows + prow;
-                    const float w = __expf(__ldcg(st.lse_part + pr) - M) * inv_den;
-                    const float* op = st.o_part + pr * D + 32 * qd;
+                    const int64_t sl = U.first_slot + pp + 1;
+                    const float w = __expf(__ldcg(st.lse_part + sl * kUnitRows + prow) - M) * inv_den;
+                    const float* op = st.o_part + (sl * D + 32 * qd) * kUnitRows + prow;
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) a[u] = fmaf(w, __ldcg(op + u), a[u]);
+                    for (int u = 0; u < 32; ++u) a[u] = fmaf(w, __ldcg(op + (int64_t)u * kUnitRows), a[u]);
                 }
                 for (int j = 2; j < t; ++j) {
                     const uint16_t* vp = st.beam_v + kvj[j] * D + 32 * qd;
