@@ -220,6 +220,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            ((uint32_t)(M >> 4) << 24);
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -549,8 +553,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
             const int ctx_len = st.req[U.req].ctx_len;
             const int n = J.t1 - J.t0;
             const bool merger = (J.slot == U.first_slot);
-            // this row's beam and query head; the beam part of its scores is computed now,
-            // while the first S tile is still being produced
+            // this row's beam and query head
             const GrReqDev& R = st.req[U.req];
             const int b = U.beam0 + i * (kTileRows / G) + row_t / G;
             const int g = row_t % G;
@@ -558,34 +561,10 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
             const bool live = row_ok && t < R.n_levels && b < st.n_beams[U.req * (st.n_levels + 1) + t];
             const int64_t orow_idx = (int64_t)(R.row_off + b) * st.n_q_heads + U.head * G + g;
             const int L = st.n_levels;
-            float sj[kMaxLevels];
+            const int32_t* path = st.path + ((int64_t)(t - 1) * st.rows + R.row_off + b) * L;
+            if (merger && live) prefetch_l2(path);
+            const int jj_pf = n > 2 ? n - 2 : 0;  // tile at which the merge inputs are prefetched
             int64_t kvj[kMaxLevels];
-            if (merger && live) {
-                const int32_t* path = st.path + ((int64_t)(t - 1) * st.rows + R.row_off + b) * L;
-                const uint4* qrow = reinterpret_cast<const uint4*>(q + orow_idx * D);
-                for (int j = 0; j < t; ++j) {
-                    kvj[j] = (((int64_t)layer * (L - 1) + j) * st.rows + R.row_off + path[j]) * st.n_kv_heads + U.head;
-                    const uint4* krow = reinterpret_cast<const uint4*>(st.beam_k + kvj[j] * D);
-                    float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-                    for (int half = 0; half < D / 64; ++half) {
-                        uint4 qa[8], ka[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) { qa[e] = __ldg(qrow + 8 * half + e); ka[e] = __ldg(krow + 8 * half + e); }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const uint32_t qw[4] = {qa[e].x, qa[e].y, qa[e].z, qa[e].w};
-                            const uint32_t kw[4] = {ka[e].x, ka[e].y, ka[e].z, ka[e].w};
-#pragma unroll
-                            for (int h2 = 0; h2 < 4; ++h2) {
-                                d0 = fmaf(__uint_as_float(qw[h2] << 16), __uint_as_float(kw[h2] << 16), d0);
-                                d1 = fmaf(__uint_as_float(qw[h2] & 0xFFFF0000u), __uint_as_float(kw[h2] & 0xFFFF0000u), d1);
-                            }
-                        }
-                    }
-                    sj[j] = (d0 + d1) * scale;
-                }
-            }
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int jj = 0; jj < n; ++jj) {
                 if (!(ok = wait_warp(bar(B_S_FULL + i), tiles & 1, wt))) break;
@@ -654,6 +633,26 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
                 tc_fence_before();
                 mbar_arrive(bar(B_P_FULL + i));
                 ++tiles;
+                if (merger && jj == jj_pf) {
+                    // two tiles before the merge: pull its inputs into L2 (ancestry-indexed
+                    // BeamKV rows, the query row, the published pieces' columns)
+                    if (live) {
+                        const char* qrow = reinterpret_cast<const char*>(q + orow_idx * D);
+                        for (int o = 0; o < D * 2; o += 128) prefetch_l2(qrow + o);
+                        for (int j = 0; j < t; ++j) {
+                            const int slot = path[j];
+                            kvj[j] = (((int64_t)layer * (L - 1) + j) * st.rows + R.row_off + slot) * st.n_kv_heads +
+                                     U.head;
+                            const char* kr = reinterpret_cast<const char*>(st.beam_k + kvj[j] * D);
+                            const char* vr = reinterpret_cast<const char*>(st.beam_v + kvj[j] * D);
+                            for (int o = 0; o < D * 2; o += 128) { prefetch_l2(kr + o); prefetch_l2(vr + o); }
+                        }
+                    }
+                    const int prow_w = i * kTileRows + quarter * 32;  // the warp's 32 rows share a line per column
+                    for (int pp = 1; pp < U.n_slots; ++pp)
+                        for (int c = lane; c < D; c += 32)
+                            prefetch_l2(st.o_part + ((int64_t)(U.first_slot + pp) * D + c) * kUnitRows + prow_w);
+                }
             }
             if (!ok) break;
             // epilogue
@@ -683,110 +682,173 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
                 continue;
             }
             // the first key range merges: the other pieces of the unit (finished earlier,
-            // at the start of their CTAs' ranges) and the beam's BeamKV tokens
-            if (!row_ok) continue;  // row of the tile beyond this request
-            uint4* dst = reinterpret_cast<uint4*>(out + orow_idx * D);
-            if (!live) {
-#pragma unroll
-                for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);  // dead beam
-                continue;
-            }
-            // wait (bounded) for the other pieces of this row
+            // at the start of their CTAs' ranges) and the beam's BeamKV tokens.  When this
+            // is the CTA's last job every S MMA has completed and nothing more is loaded, so
+            // the warp's 32 rows of V and of output pass through its share of the K stages
+            // and are read / written coalesced; otherwise thread by thread.
+            const bool staged = (jb == jr.y - 1);
+            constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per bf16 row
+            uint8_t* stg = smem + P::kKOff + (warp - 4) * 32 * D * 2;
             const int n_other = U.n_slots - 1;
-            const float* lse_col = st.lse_part + (int64_t)U.first_slot * kUnitRows + prow;
             bool have = true;
-            for (int pp = 1; pp <= n_other && have; ++pp)
-                have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, epoch, wt);
-            if (!have) { ok = false; break; }
+            if (live)
+                for (int pp = 1; pp <= n_other && have; ++pp)
+                    have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, epoch, wt);
+            if (__any_sync(0xffffffffu, !have)) { ok = false; break; }
             __threadfence();
-            constexpr int kRegPieces = 2;  // pieces merged from registers; more are streamed
-            float lse_o[kRegPieces];
-            float M = lse_own;
+            // ---- beam scores q . k_j / sqrt(D)
+            float sj[kMaxLevels];
+            for (int j = 0; j < t; ++j) {
+                const uint16_t* qp_mine = q + (live ? orow_idx : 0) * D;
+                const uint16_t* kp_mine = st.beam_k + (live ? kvj[j] : 0) * D;
+                float mine = 0.f;
+                if (staged) {
+                    // lanes split each of the warp's rows: coalesced loads, shuffle reduction
+                    constexpr int E = D / 32;
+                    for (int r0 = 0; r0 < 32; r0 += 8) {
+                        float dsum[8];
 #pragma unroll
-            for (int pp = 0; pp < kRegPieces; ++pp) {
-                lse_o[pp] = (pp < n_other) ? __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) : -CUDART_INF_F;
-                M = fmaxf(M, lse_o[pp]);
-            }
-            for (int pp = kRegPieces; pp < n_other; ++pp) M = fmaxf(M, __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows));
-            for (int j = 0; j < t; ++j) M = fmaxf(M, sj[j]);
-            const float w_own = __expf(lse_own - M);
-            float den = w_own;
-            float w_o[kRegPieces];
+                        for (int k = 0; k < 8; ++k) {
+                            const uint16_t* qp = reinterpret_cast<const uint16_t*>(
+                                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(qp_mine), r0 + k));
+                            const uint16_t* kp = reinterpret_cast<const uint16_t*>(
+                                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(kp_mine), r0 + k));
+                            float d = 0.f;
+                            if constexpr (E == 4) {
+                                const uint2 qa = __ldg(reinterpret_cast<const uint2*>(qp) + lane);
+                                const uint2 ka = __ldg(reinterpret_cast<const uint2*>(kp) + lane);
+                                d = __uint_as_float(qa.x << 16) * __uint_as_float(ka.x << 16) +
+                                    __uint_as_float(qa.x & 0xFFFF0000u) * __uint_as_float(ka.x & 0xFFFF0000u) +
+                                    __uint_as_float(qa.y << 16) * __uint_as_float(ka.y << 16) +
+                                    __uint_as_float(qa.y & 0xFFFF0000u) * __uint_as_float(ka.y & 0xFFFF0000u);
+                            } else {
+                                const uint32_t qa = __ldg(reinterpret_cast<const uint32_t*>(qp) + lane);
+                                const uint32_t ka = __ldg(reinterpret_cast<const uint32_t*>(kp) + lane);
+                                d = __uint_as_float(qa << 16) * __uint_as_float(ka << 16) +
+                                    __uint_as_float(qa & 0xFFFF0000u) * __uint_as_float(ka & 0xFFFF0000u);
+                            }
+                            dsum[k] = d;
+                        }
 #pragma unroll
-            for (int pp = 0; pp < kRegPieces; ++pp) { w_o[pp] = __expf(lse_o[pp] - M); den += w_o[pp]; }
-            for (int pp = kRegPieces; pp < n_other; ++pp) den += __expf(__ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) - M);
-            float w_j[kMaxLevels];
-            for (int j = 0; j < t; ++j) { w_j[j] = __expf(sj[j] - M); den += w_j[j]; }
-            const float inv_den = 1.f / den;
-            const float c_own = w_own * inv_l * inv_den;
+                        for (int k = 0; k < 8; ++k) {
+                            float d = dsum[k];
 #pragma unroll
-            for (int pp = 0; pp < kRegPieces; ++pp) w_o[pp] *= inv_den;
-            for (int j = 0; j < t; ++j) w_j[j] *= inv_den;
-            // 32 output columns at a time: every load of a quarter is issued before use
-#pragma unroll
-            for (int qd = 0; qd < D / 32; ++qd) {
-                float a[32];
-#pragma unroll
-                for (int u = 0; u < 32; ++u) a[u] = __uint_as_float(ov[32 * qd + u]) * c_own;
-                float pv[kRegPieces][32];
-#pragma unroll
-                for (int pp = 0; pp < kRegPieces; ++pp) {
-                    if (pp < n_other) {
-                        const float* op = st.o_part + ((int64_t)(U.first_slot + pp + 1) * D + 32 * qd) * kUnitRows + prow;
-#pragma unroll
-                        for (int u = 0; u < 32; ++u) pv[pp][u] = __ldcg(op + (int64_t)u * kUnitRows);
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 32; ++u) pv[pp][u] = 0.f;
+                            for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+                            if (lane == r0 + k) mine = d;
+                        }
                     }
-                }
-                uint4 vv[2][4];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    if (j < t) {
-                        const uint4* vp = reinterpret_cast<const uint4*>(st.beam_v + kvj[j] * D + 32 * qd);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) vv[j][e] = __ldg(vp + e);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) vv[j][e] = make_uint4(0, 0, 0, 0);
-                    }
-                }
-#pragma unroll
-                for (int pp = 0; pp < kRegPieces; ++pp)
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) a[u] = fmaf(w_o[pp], pv[pp][u], a[u]);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float wj = (j < t) ? w_j[j] : 0.f;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t vw[4] = {vv[j][e].x, vv[j][e].y, vv[j][e].z, vv[j][e].w};
+                } else if (live) {
+                    const uint4* qrow = reinterpret_cast<const uint4*>(qp_mine);
+                    const uint4* krow = reinterpret_cast<const uint4*>(kp_mine);
+                    float d0 = 0.f, d1 = 0.f;
+#pragma unroll 4
+                    for (int e = 0; e < D / 8; ++e) {
+                        const uint4 qa = __ldg(qrow + e), ka = __ldg(krow + e);
+                        const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
 #pragma unroll
                         for (int h2 = 0; h2 < 4; ++h2) {
-                            a[8 * e + 2 * h2] = fmaf(wj, __uint_as_float(vw[h2] << 16), a[8 * e + 2 * h2]);
-                            a[8 * e + 2 * h2 + 1] = fmaf(wj, __uint_as_float(vw[h2] & 0xFFFF0000u), a[8 * e + 2 * h2 + 1]);
+                            d0 = fmaf(__uint_as_float(qw[h2] << 16), __uint_as_float(kw[h2] << 16), d0);
+                            d1 = fmaf(__uint_as_float(qw[h2] & 0xFFFF0000u), __uint_as_float(kw[h2] & 0xFFFF0000u), d1);
+                        }
+                    }
+                    mine = d0 + d1;
+                }
+                sj[j] = mine * scale;
+            }
+            // ---- weights of the parts (own piece, published pieces, beam tokens)
+            const float* lse_col = st.lse_part + (int64_t)U.first_slot * kUnitRows + prow;
+            float M = lse_own;
+            for (int pp = 1; pp <= n_other; ++pp) M = fmaxf(M, __ldcg(lse_col + (int64_t)pp * kUnitRows));
+            for (int j = 0; j < t; ++j) M = fmaxf(M, sj[j]);
+            float den = __expf(lse_own - M);
+            for (int pp = 1; pp <= n_other; ++pp) den += __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
+            float w_j[kMaxLevels];
+            for (int j = 0; j < t; ++j) { w_j[j] = __expf(sj[j] - M); den += w_j[j]; }
+            // dead beams come out as exact zeros: none of their (unwritten) inputs is used
+            const float inv_den = 1.f / den;
+            const float c_own = live ? __expf(lse_own - M) * inv_l * inv_den : 0.f;
+            for (int j = 0; j < t; ++j) w_j[j] = live ? w_j[j] * inv_den : 0.f;
+            float* a = reinterpret_cast<float*>(ov);  // the row accumulates in place of O
+#pragma unroll
+            for (int c = 0; c < D; ++c) a[c] = live ? __uint_as_float(ov[c]) * c_own : 0.f;
+            // ---- published pieces: column-major, coalesced across the warp
+            for (int pp = 1; live && pp <= n_other; ++pp) {
+                const float w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M) * inv_den;
+                const float* op = st.o_part + (int64_t)(U.first_slot + pp) * D * kUnitRows + prow;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float x[32];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) x[u] = __ldcg(op + (int64_t)(c0 + u) * kUnitRows);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) a[c0 + u] = fmaf(w, x[u], a[c0 + u]);
+                }
+            }
+            // ---- BeamKV values
+            for (int j = 0; j < t; ++j) {
+                if (staged) {
+                    const uint16_t* vp_mine = st.beam_v + (live ? kvj[j] : 0) * D;
+                    __syncwarp();
+                    constexpr int kRowsPer = 32 / kChunks;  // rows one warp instruction covers
+                    for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
+                        const int r = r0 + lane / kChunks, c = lane % kChunks;
+                        const uint16_t* vp = reinterpret_cast<const uint16_t*>(
+                            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(vp_mine), r));
+                        const uint4 v = __ldg(reinterpret_cast<const uint4*>(vp) + c);
+                        *reinterpret_cast<uint4*>(stg + (r * kChunks + (c ^ (r & (kChunks - 1)))) * 16) = v;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < kChunks && live; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(
+                            stg + (lane * kChunks + (c ^ (lane & (kChunks - 1)))) * 16);
+                        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int h2 = 0; h2 < 4; ++h2) {
+                            a[8 * c + 2 * h2] = fmaf(w_j[j], __uint_as_float(vw[h2] << 16), a[8 * c + 2 * h2]);
+                            a[8 * c + 2 * h2 + 1] = fmaf(w_j[j], __uint_as_float(vw[h2] & 0xFFFF0000u), a[8 * c + 2 * h2 + 1]);
+                        }
+                    }
+                } else if (live) {
+                    const uint4* vp = reinterpret_cast<const uint4*>(st.beam_v + kvj[j] * D);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        const uint4 v = __ldg(vp + c);
+                        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int h2 = 0; h2 < 4; ++h2) {
+                            a[8 * c + 2 * h2] = fmaf(w_j[j], __uint_as_float(vw[h2] << 16), a[8 * c + 2 * h2]);
+                            a[8 * c + 2 * h2 + 1] = fmaf(w_j[j], __uint_as_float(vw[h2] & 0xFFFF0000u), a[8 * c + 2 * h2 + 1]);
                         }
                     }
                 }
-                // rare: more pieces or deeper BeamKV than the register path holds
-                for (int pp = kRegPieces; pp < n_other; ++pp) {
-                    const int64_t sl = U.first_slot + pp + 1;
-                    const float w = __expf(__ldcg(st.lse_part + sl * kUnitRows + prow) - M) * inv_den;
-                    const float* op = st.o_part + (sl * D + 32 * qd) * kUnitRows + prow;
+            }
+            // ---- bf16 output rows (rows beyond the request are another request's: not written)
+            if (staged) {
+                __syncwarp();
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) a[u] = fmaf(w, __ldcg(op + (int64_t)u * kUnitRows), a[u]);
+                for (int c = 0; c < kChunks; ++c)
+                    *reinterpret_cast<uint4*>(stg + (lane * kChunks + (c ^ (lane & (kChunks - 1)))) * 16) =
+                        make_uint4(pack_bf16x2(a[8 * c], a[8 * c + 1]), pack_bf16x2(a[8 * c + 2], a[8 * c + 3]),
+                                   pack_bf16x2(a[8 * c + 4], a[8 * c + 5]), pack_bf16x2(a[8 * c + 6], a[8 * c + 7]));
+                __syncwarp();
+                uint16_t* op_mine = out + orow_idx * D;
+                constexpr int kRowsPer = 32 / kChunks;
+                for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
+                    const int r = r0 + lane / kChunks, c = lane % kChunks;
+                    uint16_t* op = reinterpret_cast<uint16_t*>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(op_mine), r));
+                    const int ok_r = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, r);
+                    if (ok_r)
+                        reinterpret_cast<uint4*>(op)[c] =
+                            *reinterpret_cast<const uint4*>(stg + (r * kChunks + (c ^ (r & (kChunks - 1)))) * 16);
                 }
-                for (int j = 2; j < t; ++j) {
-                    const uint16_t* vp = st.beam_v + kvj[j] * D + 32 * qd;
+            } else if (row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(out + orow_idx * D);
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) a[u] = fmaf(w_j[j], __uint_as_float((uint32_t)__ldg(vp + u) << 16), a[u]);
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[4 * qd + e] = make_uint4(pack_bf16x2(a[8 * e], a[8 * e + 1]), pack_bf16x2(a[8 * e + 2], a[8 * e + 3]),
-                                                 pack_bf16x2(a[8 * e + 4], a[8 * e + 5]),
-                                                 pack_bf16x2(a[8 * e + 6], a[8 * e + 7]));
+                for (int c = 0; c < kChunks; ++c)
+                    dst[c] = make_uint4(pack_bf16x2(a[8 * c], a[8 * c + 1]), pack_bf16x2(a[8 * c + 2], a[8 * c + 3]),
+                                        pack_bf16x2(a[8 * c + 4], a[8 * c + 5]), pack_bf16x2(a[8 * c + 6], a[8 * c + 7]));
             }
         }
     }
