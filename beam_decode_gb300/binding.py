@@ -39,8 +39,9 @@ KERNEL_NAMES = ["attn", "logsoftmax_gather", "topk_select", "advance", "results"
 SYMBOLS = [
     "gr_trie_device_bytes", "gr_trie_create", "gr_trie_destroy",
     "gr_beam_workspace_bytes", "gr_beam_kv_bytes", "gr_beam_create", "gr_beam_destroy",
-    "gr_beam_rows", "gr_beam_step", "gr_beam_kv_slot", "gr_decode_attn", "gr_constrained_topk",
-    "gr_beam_advance", "gr_beam_rewind", "gr_beam_results", "gr_beam_path", "gr_beam_status",
+    "gr_beam_rows", "gr_beam_step", "gr_beam_request_step", "gr_beam_kv_slot", "gr_beam_kv_slot_request",
+    "gr_decode_attn", "gr_constrained_topk", "gr_beam_advance", "gr_beam_rewind", "gr_beam_admit",
+    "gr_beam_set_graph_mode", "gr_beam_sync", "gr_beam_results", "gr_beam_path", "gr_beam_status",
     "gr_beam_set_timing", "gr_beam_kernel_stats", "gr_beam_set_wait_limit",
     "gr_constrained_topk_noalloc", "gr_status_str", "gr_last_error",
 ]
@@ -90,11 +91,16 @@ def lib() -> ctypes.CDLL:
             "gr_beam_destroy": [vp],
             "gr_beam_rows": [vp, P(c_int), vp],
             "gr_beam_step": [vp, P(c_int)],
+            "gr_beam_request_step": [vp, c_int, P(c_int), P(c_int)],
             "gr_beam_kv_slot": [vp, c_int, P(vp), P(vp)],
+            "gr_beam_kv_slot_request": [vp, c_int, c_int, P(vp), P(vp)],
             "gr_decode_attn": [vp, c_int, vp, vp, vp],
             "gr_constrained_topk": [vp, vp, c_i64, vp, vp, vp, vp],
             "gr_beam_advance": [vp, vp],
-            "gr_beam_rewind": [vp, c_int],
+            "gr_beam_rewind": [vp, c_int, vp],
+            "gr_beam_admit": [vp, c_int, P(GrRequest), vp],
+            "gr_beam_set_graph_mode": [vp, c_int],
+            "gr_beam_sync": [vp, vp],
             "gr_beam_results": [vp, c_int, vp, vp, vp, P(c_int), vp],
             "gr_beam_path": [vp, c_int, c_int, vp, vp, vp, vp, P(c_int), vp],
             "gr_beam_status": [vp, c_int, vp],
@@ -210,12 +216,26 @@ class Beam:
         check(lib().gr_beam_step(self.handle, ctypes.byref(s)))
         return s.value
 
-    def kv_slot(self, layer: int):
-        """(k_new, v_new) views [rows, n_kv_heads, head_dim] of the open BeamKV level."""
+    def request_step(self, request: int) -> Tuple[int, int]:
+        """(t_r, L_r) of one request (host copy; call sync() after graph replays)."""
+        t, L = ctypes.c_int(), ctypes.c_int()
+        check(lib().gr_beam_request_step(self.handle, request, ctypes.byref(t), ctypes.byref(L)))
+        return t.value, L.value
+
+    def kv_slot(self, layer: int, request: Optional[int] = None):
+        """(k_new, v_new) views of the open BeamKV level: [rows, n_kv_heads, head_dim] for the
+        whole batch (all requests at one step), or [W_r, ...] of one request at its own step."""
         k, v = ctypes.c_void_p(), ctypes.c_void_p()
-        check(lib().gr_beam_kv_slot(self.handle, layer, ctypes.byref(k), ctypes.byref(v)))
-        t = self.step
-        kk, vv = self.beam_k[layer, t - 1], self.beam_v[layer, t - 1]
+        if request is None:
+            check(lib().gr_beam_kv_slot(self.handle, layer, ctypes.byref(k), ctypes.byref(v)))
+            t = max(self.request_step(r)[0] for r in range(self.n_requests)
+                    if 1 <= self.request_step(r)[0] < self.request_step(r)[1])
+            kk, vv = self.beam_k[layer, t - 1], self.beam_v[layer, t - 1]
+        else:
+            check(lib().gr_beam_kv_slot_request(self.handle, layer, request, ctypes.byref(k), ctypes.byref(v)))
+            t = self.request_step(request)[0]
+            r0, w = self.row_offsets[request], self.widths[request]
+            kk, vv = self.beam_k[layer, t - 1, r0:r0 + w], self.beam_v[layer, t - 1, r0:r0 + w]
         assert kk.data_ptr() == k.value and vv.data_ptr() == v.value
         return kk, vv
 
@@ -232,13 +252,26 @@ class Beam:
     def advance(self, stream=None) -> None:
         check(lib().gr_beam_advance(self.handle, _stream_ptr(stream)))
 
-    def rewind(self, step: int) -> None:
-        check(lib().gr_beam_rewind(self.handle, step))
+    def rewind(self, step: int, stream=None) -> None:
+        check(lib().gr_beam_rewind(self.handle, step, _stream_ptr(stream)))
+
+    def admit(self, request: int, ctx_offset: int, ctx_len: int, beam_width: int, trie: "Trie", stream=None) -> None:
+        """Slot `request` takes a new request (continuous batching); the slot's rows stay."""
+        rq = GrRequest(ctx_offset, ctx_len, beam_width, trie.handle)
+        check(lib().gr_beam_admit(self.handle, request, ctypes.byref(rq), _stream_ptr(stream)))
+        self.tries[request] = trie  # keeps the catalogue's device buffer alive
+        self.reqs[request] = rq
+
+    def set_graph_mode(self, enable: bool) -> None:
+        check(lib().gr_beam_set_graph_mode(self.handle, 1 if enable else 0))
+
+    def sync(self, stream=None) -> None:
+        check(lib().gr_beam_sync(self.handle, _stream_ptr(stream)))
 
     # -- reading back ----------------------------------------------------------
     def results(self, request: int, stream=None):
-        """(codes int32 [n, L], item_ids int64 [n], scores float32 [n])."""
-        W, L = self.widths[request], self.cfg.n_levels
+        """(codes int32 [n, L_r], item_ids int64 [n], scores float32 [n])."""
+        W, L = self.widths[request], self.request_step(request)[1]
         codes = np.zeros((W, L), dtype=np.int32)
         items = np.zeros(W, dtype=np.int64)
         scores = np.zeros(W, dtype=np.float32)

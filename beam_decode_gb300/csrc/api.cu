@@ -276,8 +276,12 @@ struct Schedule {
     std::vector<int2> cta_jobs;
 };
 
+struct Caps {
+    size_t units = 0, jobs = 0, ctas = 0;
+};
+
 struct WsLayout {
-    size_t req, row_req, n_beams, parent, token, node, score, path, cand, sel_parent, sel_code, sel_key, n_sel,
+    size_t req, row_req, req_step, n_beams, parent, token, node, score, path, cand, sel_parent, sel_code, sel_key, n_sel,
         status, tmaps, jobs, cta_jobs, units, tables_end, o_part, lse_part, piece_flag, res_codes, res_items, res_scores,
         total;
 };
@@ -308,8 +312,9 @@ gr_status check_config(const gr_config* c, const gr_request* reqs, int n) {
         if (q.beam_width < 1 || q.beam_width > kMaxBeam)
             return fail(GR_ERR_CAPACITY, "request %d: beam_width must be in 1..%d", r, kMaxBeam);
         if (q.trie == nullptr) return fail(GR_ERR_INVALID_ARG, "request %d: trie is NULL", r);
-        if (q.trie->n_levels != c->n_levels || q.trie->C != c->codes_per_level)
-            return fail(GR_ERR_INVALID_ARG, "request %d: trie levels/codes do not match the config", r);
+        if (q.trie->n_levels < 1 || q.trie->n_levels > c->n_levels || q.trie->C != c->codes_per_level)
+            return fail(GR_ERR_INVALID_ARG, "request %d: the trie needs 1..%d levels of %d codes", r, c->n_levels,
+                        c->codes_per_level);
     }
     return GR_OK;
 }
@@ -378,7 +383,7 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     return s;
 }
 
-WsLayout ws_layout(const gr_config* c, int n, int rows, const Schedule& s) {
+WsLayout ws_layout(const gr_config* c, int n, int rows, const Caps& k) {
     WsLayout w{};
     size_t o = 0;
     auto take = [&](size_t bytes, size_t align = 256) {
@@ -388,15 +393,16 @@ WsLayout ws_layout(const gr_config* c, int n, int rows, const Schedule& s) {
         return r;
     };
     const int L = c->n_levels;
-    // tables uploaded at create come first
+    // tables (uploaded at create and at every admission) come first
     w.req = take(sizeof(GrReqDev) * n);
     w.row_req = take(4ull * rows);
     w.tmaps = take(sizeof(CUtensorMap) * 2 * n, 128);
-    w.jobs = take(sizeof(GrAttnJob) * s.jobs.size());
-    w.cta_jobs = take(sizeof(int2) * s.cta_jobs.size());
-    w.units = take(sizeof(GrAttnUnit) * s.units.size());
+    w.jobs = take(sizeof(GrAttnJob) * k.jobs);
+    w.cta_jobs = take(sizeof(int2) * k.ctas);
+    w.units = take(sizeof(GrAttnUnit) * k.units);
     w.tables_end = align_up(o, 256);
     // device state
+    w.req_step = take(4ull * n);
     w.n_beams = take(4ull * n * (L + 1));
     w.parent = take(4ull * L * rows);
     w.token = take(4ull * L * rows);
@@ -409,14 +415,25 @@ WsLayout ws_layout(const gr_config* c, int n, int rows, const Schedule& s) {
     w.sel_key = take(4ull * rows);
     w.n_sel = take(4ull * n);
     w.status = take(16);
-    w.o_part = take(4ull * s.jobs.size() * kUnitRows * c->head_dim);
-    w.lse_part = take(4ull * s.jobs.size() * kUnitRows);
-    w.piece_flag = take(4ull * s.jobs.size() * kUnitRows);
+    w.o_part = take(4ull * k.jobs * kUnitRows * c->head_dim);
+    w.lse_part = take(4ull * k.jobs * kUnitRows);
+    w.piece_flag = take(4ull * k.jobs * kUnitRows);
     w.res_codes = take(4ull * rows * L);
     w.res_items = take(8ull * rows);
     w.res_scores = take(4ull * rows);
     w.total = align_up(o, 256);
     return w;
+}
+
+// Capacities of the schedule tables: admissions rebuild the schedule, and a request
+// admitted into a slot never has more beams than the slot's rows, so the units never
+// outnumber those at create; every cut of a unit adds one job, at most one per CTA.
+Caps caps_of(const Schedule& s, int n_sm) {
+    Caps k;
+    k.units = s.units.size();
+    k.ctas = (size_t)std::max(n_sm, 1);
+    k.jobs = k.units + k.ctas;
+    return k;
 }
 
 int rows_of(const gr_request* reqs, int n) {
@@ -429,16 +446,21 @@ int rows_of(const gr_request* reqs, int n) {
 struct gr_beam {
     gr_config cfg{};
     int n_req = 0, rows = 0;
-    std::vector<int> row_off;
-    std::vector<gr_request> reqs;
+    std::vector<int> row_off;     // [n_req + 1] rows of each request slot (fixed at create)
+    std::vector<gr_request> reqs; // the request each slot holds now
     gr_buffers bufs{};
     GrState st{};
     Schedule sched;
+    WsLayout w{};
+    Caps caps{};
+    std::vector<uint8_t> img;     // host image of the device tables
     int n_sm = 0;
-    // step state
-    int step = 0;
+    // host mirror of the device step state (call-order checks); graph mode leaves it alone
+    int step = 0;                 // advances since create or the last rewind
+    std::vector<int> req_step;    // t_r of each request
     std::vector<uint8_t> attn_done;
     bool topk_done = false;
+    bool graph_mode = false;
     // measurement
     bool timing = false;
     int64_t launches[GR_KERNEL_KINDS] = {};
@@ -446,7 +468,10 @@ struct gr_beam {
     std::vector<Ev> events[GR_KERNEL_KINDS];
     std::vector<Ev> event_pool;
     int64_t wait_limit_ns = 2000000000ll;
-    uint32_t attn_epoch = 0;
+
+    int levels(int r) const { return reqs[r].trie->n_levels; }
+    bool decoding(int r) const { return req_step[r] < levels(r); }
+    bool attending(int r) const { return req_step[r] >= 1 && req_step[r] < levels(r); }
 
     ~gr_beam() {
         for (int k = 0; k < GR_KERNEL_KINDS; ++k)
@@ -463,7 +488,8 @@ namespace {
 template <typename F>
 gr_status run_kernel(gr_beam* h, int kind, cudaStream_t s, F&& launch) {
     gr_beam::Ev ev{nullptr, nullptr};
-    if (h->timing) {
+    const bool timed = h->timing && !h->graph_mode;
+    if (timed) {
         if (!h->event_pool.empty()) {
             ev = h->event_pool.back();
             h->event_pool.pop_back();
@@ -479,7 +505,7 @@ gr_status run_kernel(gr_beam* h, int kind, cudaStream_t s, F&& launch) {
         return cuda_fail(e, "kernel launch");
     }
     ++h->launches[kind];
-    if (h->timing) {
+    if (timed) {
         GR_CUDA(cudaEventRecord(ev.b, s), "event record");
         h->events[kind].push_back(ev);
     }
@@ -489,6 +515,63 @@ gr_status run_kernel(gr_beam* h, int kind, cudaStream_t s, F&& launch) {
 gr_status status_from_word(int w) {
     if (w & kStatusTimeout) return fail(GR_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", w);
     if (w & (kStatusNanKey | kStatusBadNode)) return fail(GR_ERR_DEVICE, "a kernel flagged invalid data (status 0x%x)", w);
+    return GR_OK;
+}
+
+// (Re)build the attention schedule for the requests the slots hold now and write the
+// host image of every device table; the caller uploads it with one copy.
+gr_status build_tables(gr_beam* h) {
+    const gr_config* cfg = &h->cfg;
+    std::vector<int> unit_off, n_ub;
+    Schedule sc = build_schedule(cfg, h->reqs.data(), h->n_req, h->n_sm, unit_off, n_ub);
+    if (sc.units.size() > h->caps.units || sc.jobs.size() > h->caps.jobs || sc.cta_jobs.size() > h->caps.ctas)
+        return fail(GR_ERR_CAPACITY, "attention schedule exceeds the workspace's tables");
+    h->sched = std::move(sc);
+    const WsLayout& w = h->w;
+    h->img.assign(w.tables_end, 0);
+    uint8_t* img = h->img.data();
+    GrReqDev* rq = reinterpret_cast<GrReqDev*>(img + w.req);
+    int32_t* rr = reinterpret_cast<int32_t*>(img + w.row_req);
+    for (int r = 0; r < h->n_req; ++r) {
+        const gr_request& q = h->reqs[r];
+        const gr_trie* t = q.trie;
+        GrReqDev d{};
+        d.row_off = h->row_off[r];
+        d.width = q.beam_width;
+        d.ctx_len = q.ctx_len;
+        d.n_levels = t->n_levels;
+        d.unit_off = unit_off[r];
+        d.n_ub = n_ub[r];
+        d.mask_words = t->mask_words;
+        d.ctx_off = q.ctx_offset;
+        d.leaf_base = t->leaf_base;
+        d.n_nodes = t->n_inner;
+        d.mask = t->mask;
+        d.child_base = t->child_base;
+        d.leaf_item = t->leaf_item;
+        rq[r] = d;
+        for (int b = h->row_off[r]; b < h->row_off[r + 1]; ++b) rr[b] = r;
+    }
+    CUtensorMap* tm = reinterpret_cast<CUtensorMap*>(img + w.tmaps);
+    const int D = cfg->head_dim;
+    const uint64_t zdim = (uint64_t)cfg->n_layers * cfg->n_kv_heads;
+    for (int r = 0; r < h->n_req; ++r) {
+        const gr_request& q = h->reqs[r];
+        const uint64_t off = (uint64_t)q.ctx_offset * D * 2;
+        const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)cfg->pool_tokens * D * 2;
+        gr_status s;
+        if ((s = make_tmap_3d(&tm[2 * r], static_cast<const uint8_t*>(h->bufs.ctx_k) + off, D, q.ctx_len, zdim, s1, s2,
+                              64, kTileKeys, 1)) != GR_OK ||
+            (s = make_tmap_3d(&tm[2 * r + 1], static_cast<const uint8_t*>(h->bufs.ctx_v) + off, D, q.ctx_len, zdim, s1,
+                              s2, 64, kTileKeys, 1)) != GR_OK)
+            return s;
+    }
+    memcpy(img + w.jobs, h->sched.jobs.data(), sizeof(GrAttnJob) * h->sched.jobs.size());
+    memcpy(img + w.cta_jobs, h->sched.cta_jobs.data(), sizeof(int2) * h->sched.cta_jobs.size());
+    memcpy(img + w.units, h->sched.units.data(), sizeof(GrAttnUnit) * h->sched.units.size());
+    h->st.n_units = (int)h->sched.units.size();
+    h->st.n_jobs = (int)h->sched.jobs.size();
+    h->st.n_cta = (int)h->sched.cta_jobs.size();
     return GR_OK;
 }
 }  // namespace
@@ -502,7 +585,7 @@ extern "C" gr_status gr_beam_workspace_bytes(const gr_config* cfg, const gr_requ
     if (n_sm <= 0) n_sm = 148;
     std::vector<int> uo, nu;
     Schedule sc = build_schedule(cfg, reqs, n_requests, n_sm, uo, nu);
-    *bytes = ws_layout(cfg, n_requests, rows_of(reqs, n_requests), sc).total;
+    *bytes = ws_layout(cfg, n_requests, rows_of(reqs, n_requests), caps_of(sc, n_sm)).total;
     return GR_OK;
 }
 
@@ -545,8 +628,9 @@ extern "C" gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs
         h->row_off[0] = 0;
         for (int r = 0; r < n_requests; ++r) h->row_off[r + 1] = h->row_off[r] + reqs[r].beam_width;
         std::vector<int> unit_off, n_ub;
-        h->sched = build_schedule(cfg, reqs, n_requests, n_sm, unit_off, n_ub);
-        const WsLayout w = ws_layout(cfg, n_requests, h->rows, h->sched);
+        h->caps = caps_of(build_schedule(cfg, reqs, n_requests, n_sm, unit_off, n_ub), n_sm);
+        h->w = ws_layout(cfg, n_requests, h->rows, h->caps);
+        const WsLayout& w = h->w;
         if (bufs->workspace_bytes < w.total) {
             gr_status e = fail(GR_ERR_CAPACITY, "workspace needs %zu bytes, got %zu", w.total, bufs->workspace_bytes);
             delete h;
@@ -567,6 +651,7 @@ extern "C" gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs
         st.head_dim = cfg->head_dim;
         st.pool_tokens = cfg->pool_tokens;
         st.row_req = reinterpret_cast<int32_t*>(ws + w.row_req);
+        st.req_step = reinterpret_cast<int32_t*>(ws + w.req_step);
         st.n_beams = reinterpret_cast<int32_t*>(ws + w.n_beams);
         st.parent = reinterpret_cast<int32_t*>(ws + w.parent);
         st.token = reinterpret_cast<int32_t*>(ws + w.token);
@@ -584,9 +669,6 @@ extern "C" gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs
         st.cta_jobs = reinterpret_cast<int2*>(ws + w.cta_jobs);
         st.units = reinterpret_cast<GrAttnUnit*>(ws + w.units);
         st.piece_flag = reinterpret_cast<uint32_t*>(ws + w.piece_flag);
-        st.n_units = (int)h->sched.units.size();
-        st.n_jobs = (int)h->sched.jobs.size();
-        st.n_cta = (int)h->sched.cta_jobs.size();
         st.o_part = reinterpret_cast<float*>(ws + w.o_part);
         st.lse_part = reinterpret_cast<float*>(ws + w.lse_part);
         st.beam_k = static_cast<const uint16_t*>(bufs->beam_k);
@@ -594,56 +676,20 @@ extern "C" gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs
         st.res_codes = reinterpret_cast<int32_t*>(ws + w.res_codes);
         st.res_items = reinterpret_cast<int64_t*>(ws + w.res_items);
         st.res_scores = reinterpret_cast<float*>(ws + w.res_scores);
-
-        // host images of the device tables, uploaded with one copy
-        std::vector<uint8_t> img(w.tables_end, 0);
-        GrReqDev* rq = reinterpret_cast<GrReqDev*>(img.data() + w.req);
-        int32_t* rr = reinterpret_cast<int32_t*>(img.data() + w.row_req);
-        for (int r = 0; r < n_requests; ++r) {
-            const gr_trie* t = reqs[r].trie;
-            GrReqDev d{};
-            d.row_off = h->row_off[r];
-            d.width = reqs[r].beam_width;
-            d.ctx_len = reqs[r].ctx_len;
-            d.n_levels = t->n_levels;
-            d.unit_off = unit_off[r];
-            d.n_ub = n_ub[r];
-            d.mask_words = t->mask_words;
-            d.ctx_off = reqs[r].ctx_offset;
-            d.leaf_base = t->leaf_base;
-            d.n_nodes = t->n_inner;
-            d.mask = t->mask;
-            d.child_base = t->child_base;
-            d.leaf_item = t->leaf_item;
-            rq[r] = d;
-            for (int b = 0; b < reqs[r].beam_width; ++b) rr[h->row_off[r] + b] = r;
+        if ((s = build_tables(h)) != GR_OK) {
+            delete h;
+            return s;
         }
-        CUtensorMap* tm = reinterpret_cast<CUtensorMap*>(img.data() + w.tmaps);
-        const int D = cfg->head_dim;
-        const uint64_t zdim = (uint64_t)cfg->n_layers * cfg->n_kv_heads;
-        for (int r = 0; r < n_requests; ++r) {
-            const uint64_t off = (uint64_t)reqs[r].ctx_offset * D * 2;
-            const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)cfg->pool_tokens * D * 2;
-            if ((s = make_tmap_3d(&tm[2 * r], static_cast<const uint8_t*>(bufs->ctx_k) + off, D, reqs[r].ctx_len,
-                                  zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK ||
-                (s = make_tmap_3d(&tm[2 * r + 1], static_cast<const uint8_t*>(bufs->ctx_v) + off, D, reqs[r].ctx_len,
-                                  zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK) {
-                delete h;
-                return s;
-            }
-        }
-        memcpy(img.data() + w.jobs, h->sched.jobs.data(), sizeof(GrAttnJob) * h->sched.jobs.size());
-        memcpy(img.data() + w.cta_jobs, h->sched.cta_jobs.data(), sizeof(int2) * h->sched.cta_jobs.size());
-        memcpy(img.data() + w.units, h->sched.units.data(), sizeof(GrAttnUnit) * h->sched.units.size());
-        cudaError_t e = cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, cs);
-        if (e == cudaSuccess) e = cudaMemsetAsync(st.piece_flag, 0, 4ull * h->sched.jobs.size() * kUnitRows, cs);
+        cudaError_t e = cudaMemcpyAsync(ws, h->img.data(), h->img.size(), cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaMemsetAsync(st.piece_flag, 0, 4ull * h->caps.jobs * kUnitRows, cs);
         if (e == cudaSuccess) e = launch_init_state(st, cs);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);  // img is released on return
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
         if (e != cudaSuccess) {
             delete h;
             return cuda_fail(e, "workspace upload");
         }
         h->launches[GR_KERNEL_INIT] += 1;
+        h->req_step.assign(n_requests, 0);
         h->attn_done.assign(cfg->n_layers, 0);
     } catch (const std::bad_alloc&) {
         delete h;
@@ -672,15 +718,48 @@ extern "C" gr_status gr_beam_step(const gr_beam* h, int* step) {
     return GR_OK;
 }
 
+extern "C" gr_status gr_beam_request_step(const gr_beam* h, int request, int* step, int* n_levels) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    if (request < 0 || request >= h->n_req) return fail(GR_ERR_INVALID_ARG, "request %d out of range", request);
+    if (step) *step = h->req_step[request];
+    if (n_levels) *n_levels = h->levels(request);
+    return GR_OK;
+}
+
+namespace {
+// BeamKV rows [row0, row0 + n) of `layer` at `level`
+void kv_view(const gr_beam* h, int layer, int level, int row0, void** k, void** v) {
+    const gr_config& c = h->cfg;
+    const size_t off =
+        ((((size_t)layer * (c.n_levels - 1) + level) * h->rows) + row0) * c.n_kv_heads * c.head_dim * 2;
+    *k = static_cast<uint8_t*>(h->bufs.beam_k) + off;
+    *v = static_cast<uint8_t*>(h->bufs.beam_v) + off;
+}
+}  // namespace
+
 extern "C" gr_status gr_beam_kv_slot(gr_beam* h, int layer, void** k_new, void** v_new) {
     if (h == nullptr || k_new == nullptr || v_new == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
     if (layer < 0 || layer >= h->cfg.n_layers) return fail(GR_ERR_INVALID_ARG, "layer %d out of range", layer);
-    if (h->step < 1 || h->step >= h->cfg.n_levels)
-        return fail(GR_ERR_STATE, "no BeamKV level is open at step %d", h->step);
-    const gr_config& c = h->cfg;
-    const size_t off = (((size_t)layer * (c.n_levels - 1) + (h->step - 1)) * h->rows) * c.n_kv_heads * c.head_dim * 2;
-    *k_new = static_cast<uint8_t*>(h->bufs.beam_k) + off;
-    *v_new = static_cast<uint8_t*>(h->bufs.beam_v) + off;
+    int t = -1;
+    for (int r = 0; r < h->n_req; ++r) {
+        if (!h->attending(r)) continue;
+        if (t >= 0 && h->req_step[r] != t)
+            return fail(GR_ERR_STATE, "requests decode different levels: use gr_beam_kv_slot_request");
+        t = h->req_step[r];
+    }
+    if (t < 1) return fail(GR_ERR_STATE, "no request has a BeamKV level open");
+    kv_view(h, layer, t - 1, 0, k_new, v_new);
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_kv_slot_request(gr_beam* h, int layer, int request, void** k_new, void** v_new) {
+    if (h == nullptr || k_new == nullptr || v_new == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (layer < 0 || layer >= h->cfg.n_layers) return fail(GR_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (request < 0 || request >= h->n_req) return fail(GR_ERR_INVALID_ARG, "request %d out of range", request);
+    if (!h->attending(request))
+        return fail(GR_ERR_STATE, "request %d has no BeamKV level open (step %d of %d)", request, h->req_step[request],
+                    h->levels(request));
+    kv_view(h, layer, h->req_step[request] - 1, h->row_off[request], k_new, v_new);
     return GR_OK;
 }
 
@@ -689,10 +768,13 @@ extern "C" gr_status gr_decode_attn(gr_beam* h, int layer, const void* q, void* 
     if (layer < 0 || layer >= h->cfg.n_layers) return fail(GR_ERR_INVALID_ARG, "layer %d out of range", layer);
     if ((reinterpret_cast<uintptr_t>(q) & 15) != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0)
         return fail(GR_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
-    if (h->step < 1 || h->step >= h->cfg.n_levels)
-        return fail(GR_ERR_STATE, "attention runs at steps 1..%d (current step %d)", h->cfg.n_levels - 1, h->step);
-    if (h->topk_done) return fail(GR_ERR_STATE, "top-K of this step already ran; call gr_beam_advance");
-    if (h->attn_done[layer]) return fail(GR_ERR_STATE, "layer %d already ran at step %d", layer, h->step);
+    if (!h->graph_mode) {
+        bool any = false;
+        for (int r = 0; r < h->n_req; ++r) any = any || h->attending(r);
+        if (!any) return fail(GR_ERR_STATE, "no request is at a decode step 1..L-1 (step %d)", h->step);
+        if (h->topk_done) return fail(GR_ERR_STATE, "top-K of this step already ran; call gr_beam_advance");
+        if (h->attn_done[layer]) return fail(GR_ERR_STATE, "layer %d already ran at step %d", layer, h->step);
+    }
     const gr_config& c = h->cfg;
     const int G = c.n_q_heads / c.n_kv_heads;
     CUtensorMap qmap;
@@ -701,14 +783,12 @@ extern "C" gr_status gr_decode_attn(gr_beam* h, int layer, const void* q, void* 
     if (s != GR_OK) return s;
     cudaStream_t cs = (cudaStream_t)stream;
     const int64_t lim = h->wait_limit_ns;
-    const int t = h->step;
-    const uint32_t epoch = ++h->attn_epoch;  // tags the pieces this launch publishes
     if ((s = run_kernel(h, GR_KERNEL_ATTN, cs, [&] {
-             return launch_ctx_attn(h->st, qmap, layer, t, static_cast<const uint16_t*>(q),
-                                    static_cast<uint16_t*>(out), epoch, lim, cs);
+             return launch_ctx_attn(h->st, qmap, layer, static_cast<const uint16_t*>(q), static_cast<uint16_t*>(out),
+                                    lim, cs);
          })) != GR_OK)
         return s;
-    h->attn_done[layer] = 1;
+    if (!h->graph_mode) h->attn_done[layer] = 1;
     return GR_OK;
 }
 
@@ -717,41 +797,113 @@ extern "C" gr_status gr_constrained_topk(gr_beam* h, const float* logits, int64_
     if (h == nullptr || logits == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
     if (ld < h->cfg.vocab || ld % 4 != 0) return fail(GR_ERR_INVALID_ARG, "ld must be >= vocab and a multiple of 4");
     if ((reinterpret_cast<uintptr_t>(logits) & 15) != 0) return fail(GR_ERR_INVALID_ARG, "logits must be 16-byte aligned");
-    if (h->step >= h->cfg.n_levels) return fail(GR_ERR_STATE, "decoding is finished");
-    if (h->topk_done) return fail(GR_ERR_STATE, "top-K already ran at step %d; call gr_beam_advance", h->step);
+    if (!h->graph_mode) {
+        bool any = false;
+        for (int r = 0; r < h->n_req; ++r) any = any || h->decoding(r);
+        if (!any) return fail(GR_ERR_STATE, "decoding is finished for every request");
+        if (h->topk_done) return fail(GR_ERR_STATE, "top-K already ran at step %d; call gr_beam_advance", h->step);
+    }
     cudaStream_t cs = (cudaStream_t)stream;
-    const int t = h->step;
     gr_status s;
     if ((s = run_kernel(h, GR_KERNEL_LOGSOFTMAX, cs, [&] {
-             return launch_logsoftmax_gather(h->st, t, logits, ld, logprobs_out, lse_out, lse_in, cs);
+             return launch_logsoftmax_gather(h->st, logits, ld, logprobs_out, lse_out, lse_in, cs);
          })) != GR_OK)
         return s;
-    if ((s = run_kernel(h, GR_KERNEL_TOPK, cs, [&] { return launch_topk_select(h->st, t, cs); })) != GR_OK) return s;
-    h->topk_done = true;
+    if ((s = run_kernel(h, GR_KERNEL_TOPK, cs, [&] { return launch_topk_select(h->st, cs); })) != GR_OK) return s;
+    if (!h->graph_mode) h->topk_done = true;
     return GR_OK;
 }
 
 extern "C" gr_status gr_beam_advance(gr_beam* h, gr_stream_t stream) {
     if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
-    if (!h->topk_done) return fail(GR_ERR_STATE, "gr_constrained_topk has not run at step %d", h->step);
+    if (!h->graph_mode && !h->topk_done)
+        return fail(GR_ERR_STATE, "gr_constrained_topk has not run at step %d", h->step);
     cudaStream_t cs = (cudaStream_t)stream;
-    const int t = h->step;
-    gr_status s = run_kernel(h, GR_KERNEL_ADVANCE, cs, [&] { return launch_advance(h->st, t, cs); });
+    gr_status s = run_kernel(h, GR_KERNEL_ADVANCE, cs, [&] { return launch_advance(h->st, cs); });
     if (s != GR_OK) return s;
-    h->step = t + 1;
-    h->topk_done = false;
-    std::fill(h->attn_done.begin(), h->attn_done.end(), 0);
+    if (!h->graph_mode) {
+        for (int r = 0; r < h->n_req; ++r)
+            if (h->decoding(r)) ++h->req_step[r];
+        h->step += 1;
+        h->topk_done = false;
+        std::fill(h->attn_done.begin(), h->attn_done.end(), 0);
+    }
     return GR_OK;
 }
 
-extern "C" gr_status gr_beam_rewind(gr_beam* h, int step) {
+extern "C" gr_status gr_beam_rewind(gr_beam* h, int step, gr_stream_t stream) {
     if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
-    if (step < 0 || step > h->step)
+    if (step < 0) return fail(GR_ERR_INVALID_ARG, "step must be >= 0");
+    if (!h->graph_mode && step > h->step)
         return fail(GR_ERR_STATE, "can rewind only to a decoded step 0..%d (asked %d)", h->step, step);
-    h->step = step;
+    cudaStream_t cs = (cudaStream_t)stream;
+    gr_status s = run_kernel(h, GR_KERNEL_INIT, cs, [&] { return launch_set_step(h->st, step, cs); });
+    if (s != GR_OK) return s;
+    if (!h->graph_mode) {
+        for (int r = 0; r < h->n_req; ++r) h->req_step[r] = std::min(h->req_step[r], step);
+        h->step = std::min(h->step, step);
+        h->topk_done = false;
+        std::fill(h->attn_done.begin(), h->attn_done.end(), 0);
+    }
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_admit(gr_beam* h, int request, const gr_request* req, gr_stream_t stream) {
+    if (h == nullptr || req == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (h->graph_mode) return fail(GR_ERR_STATE, "admission needs the host step state: leave graph mode first");
+    if (request < 0 || request >= h->n_req) return fail(GR_ERR_INVALID_ARG, "request %d out of range", request);
+    if (h->topk_done || std::any_of(h->attn_done.begin(), h->attn_done.end(), [](uint8_t d) { return d != 0; }))
+        return fail(GR_ERR_STATE, "admission happens between steps");
+    if (h->req_step[request] != 0 && h->decoding(request))
+        return fail(GR_ERR_STATE, "slot %d still decodes (step %d of %d)", request, h->req_step[request],
+                    h->levels(request));
+    const int slot_rows = h->row_off[request + 1] - h->row_off[request];
+    if (req->beam_width < 1 || req->beam_width > slot_rows)
+        return fail(GR_ERR_CAPACITY, "beam_width %d does not fit slot %d (%d rows)", req->beam_width, request, slot_rows);
+    gr_status s = check_config(&h->cfg, req, 1);
+    if (s != GR_OK) return s;
+    const gr_request keep = h->reqs[request];
+    h->reqs[request] = *req;
+    if ((s = build_tables(h)) != GR_OK) {
+        h->reqs[request] = keep;
+        build_tables(h);
+        return s;
+    }
+    cudaStream_t cs = (cudaStream_t)stream;
+    // the tables are small: one copy of the whole image, ordered after the work already
+    // queued on the stream (which still reads the old tables)
+    GR_CUDA(cudaMemcpyAsync(h->bufs.workspace, h->img.data(), h->img.size(), cudaMemcpyHostToDevice, cs), "admit");
+    if ((s = run_kernel(h, GR_KERNEL_INIT, cs, [&] { return launch_init_request(h->st, request, cs); })) != GR_OK)
+        return s;
+    h->req_step[request] = 0;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_set_graph_mode(gr_beam* h, int enable) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    if (enable && (h->topk_done || std::any_of(h->attn_done.begin(), h->attn_done.end(), [](uint8_t d) { return d; })))
+        return fail(GR_ERR_STATE, "graph mode starts between steps");
+    h->graph_mode = enable != 0;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_sync(gr_beam* h, gr_stream_t stream) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    cudaStream_t cs = (cudaStream_t)stream;
+    std::vector<int32_t> t(h->n_req);
+    int w = 0;
+    GR_CUDA(cudaMemcpyAsync(t.data(), h->st.req_step, 4ull * h->n_req, cudaMemcpyDeviceToHost, cs), "sync");
+    GR_CUDA(cudaMemcpyAsync(&w, h->st.status, 4, cudaMemcpyDeviceToHost, cs), "status read");
+    GR_CUDA(cudaStreamSynchronize(cs), "sync");
+    int steps = 0;
+    for (int r = 0; r < h->n_req; ++r) {
+        steps = std::max(steps, t[r] - h->req_step[r]);
+        h->req_step[r] = t[r];
+    }
+    h->step += steps;
     h->topk_done = false;
     std::fill(h->attn_done.begin(), h->attn_done.end(), 0);
-    return GR_OK;
+    return status_from_word(w);
 }
 
 extern "C" gr_status gr_beam_status(gr_beam* h, int clear_flag, gr_stream_t stream) {
@@ -761,7 +913,9 @@ extern "C" gr_status gr_beam_status(gr_beam* h, int clear_flag, gr_stream_t stre
     GR_CUDA(cudaMemcpyAsync(&w, h->st.status, 4, cudaMemcpyDeviceToHost, cs), "status read");
     GR_CUDA(cudaStreamSynchronize(cs), "status sync");
     if (clear_flag && w != 0) {
+        // a kernel that gave up may have left piece flags set: clear them with the status
         GR_CUDA(cudaMemsetAsync(h->st.status, 0, 16, cs), "status clear");
+        GR_CUDA(cudaMemsetAsync(h->st.piece_flag, 0, 4ull * h->caps.jobs * kUnitRows, cs), "flag clear");
         GR_CUDA(cudaStreamSynchronize(cs), "status clear sync");
     }
     return status_from_word(w);
@@ -771,21 +925,23 @@ extern "C" gr_status gr_beam_results(gr_beam* h, int request, int32_t* codes, in
                                      int* n_out, gr_stream_t stream) {
     if (h == nullptr || n_out == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
     if (request < 0 || request >= h->n_req) return fail(GR_ERR_INVALID_ARG, "request %d out of range", request);
-    if (h->step < h->cfg.n_levels) return fail(GR_ERR_STATE, "decoding is not finished (step %d of %d)", h->step,
-                                               h->cfg.n_levels);
+    const int Lr = h->levels(request);
+    if (h->req_step[request] < Lr)
+        return fail(GR_ERR_STATE, "request %d is not finished (step %d of %d)", request, h->req_step[request], Lr);
     cudaStream_t cs = (cudaStream_t)stream;
     gr_status s = run_kernel(h, GR_KERNEL_RESULTS, cs, [&] { return launch_results(h->st, cs); });
     if (s != GR_OK) return s;
     const int L = h->cfg.n_levels;
     int n = 0, w = 0;
-    GR_CUDA(cudaMemcpyAsync(&n, h->st.n_beams + request * (L + 1) + L, 4, cudaMemcpyDeviceToHost, cs), "results");
+    GR_CUDA(cudaMemcpyAsync(&n, h->st.n_beams + request * (L + 1) + Lr, 4, cudaMemcpyDeviceToHost, cs), "results");
     GR_CUDA(cudaMemcpyAsync(&w, h->st.status, 4, cudaMemcpyDeviceToHost, cs), "status read");
     GR_CUDA(cudaStreamSynchronize(cs), "results sync");
     if ((s = status_from_word(w)) != GR_OK) return s;
     const int row0 = h->row_off[request];
     if (n > 0) {
-        if (codes)
-            GR_CUDA(cudaMemcpyAsync(codes, h->st.res_codes + (size_t)row0 * L, 4ull * n * L, cudaMemcpyDeviceToHost, cs),
+        if (codes)  // rows of L_r codes, packed
+            GR_CUDA(cudaMemcpy2DAsync(codes, 4ull * Lr, h->st.res_codes + (size_t)row0 * L, 4ull * L, 4ull * Lr, n,
+                                      cudaMemcpyDeviceToHost, cs),
                     "results");
         if (item_ids)
             GR_CUDA(cudaMemcpyAsync(item_ids, h->st.res_items + row0, 8ull * n, cudaMemcpyDeviceToHost, cs), "results");
@@ -801,7 +957,9 @@ extern "C" gr_status gr_beam_path(gr_beam* h, int request, int level, int32_t* p
                                   int32_t* nodes, float* scores, int* n_out, gr_stream_t stream) {
     if (h == nullptr || n_out == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
     if (request < 0 || request >= h->n_req) return fail(GR_ERR_INVALID_ARG, "request %d out of range", request);
-    if (level < 0 || level >= h->step) return fail(GR_ERR_STATE, "level %d is not committed (step %d)", level, h->step);
+    if (level < 0 || level >= h->req_step[request])
+        return fail(GR_ERR_STATE, "level %d of request %d is not committed (step %d)", level, request,
+                    h->req_step[request]);
     cudaStream_t cs = (cudaStream_t)stream;
     const int L = h->cfg.n_levels;
     int n = 0, w = 0;

@@ -30,7 +30,7 @@ struct GrReqDev {
     int row_off;        // first row of the request
     int width;          // W_r
     int ctx_len;        // T_r
-    int n_levels;       // L_r (== cfg.n_levels)
+    int n_levels;       // L_r (<= cfg.n_levels; the levels of the request's trie)
     int unit_off;       // first attention unit of the request
     int n_ub;           // units per KV head: ceil(W_r * G / kUnitRows)
     int mask_words;     // 32-bit words per trie node mask
@@ -74,6 +74,8 @@ struct GrState {
     int64_t pool_tokens;
 
     int32_t* row_req;   // [rows] request of each row
+    int32_t* req_step;  // [n_req] t_r: the level each request decodes next (t_r == L_r: finished);
+                        // kernels read it, k_advance moves it, so steps replay without the host
     int32_t* n_beams;   // [n_req][L+1] live beams entering step t
     int32_t* parent;    // [L][rows] BeamPath: parent slot at level t-1
     int32_t* token;     // [L][rows]
@@ -95,7 +97,7 @@ struct GrState {
     int n_units, n_jobs, n_cta;
     float* o_part;      // [n_jobs][D][kUnitRows] pieces of split units (later key ranges), column-major
     float* lse_part;    // [n_jobs][kUnitRows]
-    uint32_t* piece_flag; // [n_jobs][kUnitRows] launch epoch of the last published piece row
+    uint32_t* piece_flag; // [n_jobs][kUnitRows] 1 = piece row published and not yet merged
     const uint16_t* beam_k; // bf16 [NL][L-1][rows][Hkv][D]
     const uint16_t* beam_v;
 
@@ -107,16 +109,18 @@ struct GrState {
 
 // ---- launchers (k_topk.cu) ----
 cudaError_t launch_init_state(const GrState& st, cudaStream_t s);
-cudaError_t launch_logsoftmax_gather(const GrState& st, int t, const float* logits, int64_t ld,
+cudaError_t launch_init_request(const GrState& st, int r, cudaStream_t s);
+cudaError_t launch_set_step(const GrState& st, int step, cudaStream_t s);
+cudaError_t launch_logsoftmax_gather(const GrState& st, const float* logits, int64_t ld,
                                      float* logprobs_out, float* lse_out, const float* lse_in,
                                      cudaStream_t s);
-cudaError_t launch_topk_select(const GrState& st, int t, cudaStream_t s);
-cudaError_t launch_advance(const GrState& st, int t, cudaStream_t s);
+cudaError_t launch_topk_select(const GrState& st, cudaStream_t s);
+cudaError_t launch_advance(const GrState& st, cudaStream_t s);
 cudaError_t launch_results(const GrState& st, cudaStream_t s);
 
 // ---- launchers (k_attn.cu) ----
 cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes);
-cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, int t, const uint16_t* q,
-                            uint16_t* out, uint32_t epoch, int64_t wait_limit_ns, cudaStream_t s);
+cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
+                            uint16_t* out, int64_t wait_limit_ns, cudaStream_t s);
 
 }  // namespace grb

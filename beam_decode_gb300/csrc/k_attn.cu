@@ -31,8 +31,8 @@
 // Epilogue: a unit whose key tiles were cut over several CTAs is finished by
 // its first key range, which by construction of the schedule is the last job
 // of its CTA; the later ranges run at the start of the next CTAs and publish
-// their normalised fp32 piece, its log-sum-exp and a per-row ready flag
-// tagged with the launch epoch.  The first range merges them with its own O
+// their normalised fp32 piece, its log-sum-exp and a per-row ready flag,
+// which the merger clears once it has read the row.  The first range merges them with its own O
 // (still in registers) and with the beam part -- the t BeamKV keys found
 // through the beam's ancestry row (levels 0..t-1) -- by a log-sum-exp
 // combine, and writes the bf16 output row.  Rows of dead beams are written
@@ -310,6 +310,14 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t value, 
     return true;
 }
 
+// a unit takes part in a launch when its request is at a decode step 1 <= t_r < L_r
+// (level 0 has no BeamKV and needs no attention; t_r == L_r is finished).  Every role of
+// the CTA reads the same device-resident step, so they skip the same jobs.
+__device__ __forceinline__ bool decoding(const GrState& st, const GrAttnUnit& U) {
+    const int t = st.req_step[U.req];
+    return t >= 1 && t < st.req[U.req].n_levels;
+}
+
 // ---------------------------------------------------------------------------
 // shared-memory plan
 // ---------------------------------------------------------------------------
@@ -341,8 +349,8 @@ constexpr int kAttnThreads = 384;
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int t, const uint16_t* __restrict__ q,
-           uint16_t* __restrict__ out, uint32_t epoch, float scale_log2, float scale, int64_t wait_limit_ns) {
+k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, const uint16_t* __restrict__ q,
+           uint16_t* __restrict__ out, float scale_log2, float scale, int64_t wait_limit_ns) {
     using P = Plan<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -397,6 +405,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
                 const GrAttnJob J = st.jobs[jb];
                 const GrAttnUnit U = st.units[J.unit];
                 const GrReqDev& R = st.req[U.req];
+                if (!decoding(st, U)) continue;
                 const CUtensorMap* km = st.tmaps + 2 * U.req;
                 const CUtensorMap* vm = km + 1;
                 if (jb == jr.x || st.jobs[jb - 1].unit != J.unit) {
@@ -460,6 +469,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
             for (int jb = jr.x; jb < jr.y && ok; ++jb) {
                 const GrAttnJob J = st.jobs[jb];
                 const GrAttnUnit U = st.units[J.unit];
+                if (!decoding(st, U)) continue;
                 const int nqt = U.nqt;
                 const int n = J.t1 - J.t0;
                 if (!(ok = wait1(bar(B_Q_FULL), qcnt & 1, wt))) break;
@@ -549,7 +559,8 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
         for (int jb = jr.x; jb < jr.y && ok; ++jb) {
             const GrAttnJob J = st.jobs[jb];
             const GrAttnUnit U = st.units[J.unit];
-            if (i >= U.nqt) continue;
+            if (i >= U.nqt || !decoding(st, U)) continue;
+            const int t = st.req_step[U.req];  // 1 <= t < L_r: BeamKV levels 0..t-1 exist
             const int ctx_len = st.req[U.req].ctx_len;
             const int n = J.t1 - J.t0;
             const bool merger = (J.slot == U.first_slot);
@@ -558,7 +569,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
             const int b = U.beam0 + i * (kTileRows / G) + row_t / G;
             const int g = row_t % G;
             const bool row_ok = b < R.width;
-            const bool live = row_ok && t < R.n_levels && b < st.n_beams[U.req * (st.n_levels + 1) + t];
+            const bool live = row_ok && b < st.n_beams[U.req * (st.n_levels + 1) + t];
             const int64_t orow_idx = (int64_t)(R.row_off + b) * st.n_q_heads + U.head * G + g;
             const int L = st.n_levels;
             const int32_t* path = st.path + ((int64_t)(t - 1) * st.rows + R.row_off + b) * L;
@@ -670,15 +681,19 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
             const int piece = J.slot - U.first_slot;
             if (piece != 0) {
                 // a later key range of a split unit: publish the normalised piece and its
-                // log-sum-exp, then this row's ready flag (tagged with the launch epoch)
-                // column-major piece [slot][D][256 rows]: a warp stores 32 consecutive rows of
-                // one column per instruction (one 128-byte transaction)
-                float* ocol = st.o_part + (int64_t)J.slot * D * kUnitRows + prow;
+                // log-sum-exp, then this row's ready flag; the merger clears the flag once it
+                // has read the row, so flags need no per-launch tag and a captured step replays.
+                // Only live rows are published (the merger reads no other row).
+                // Column-major piece [slot][D][256 rows]: a warp stores 32 consecutive rows of
+                // one column per instruction (one 128-byte transaction).
+                if (live) {
+                    float* ocol = st.o_part + (int64_t)J.slot * D * kUnitRows + prow;
 #pragma unroll
-                for (int c = 0; c < D; ++c) __stcg(ocol + (int64_t)c * kUnitRows, __uint_as_float(ov[c]) * inv_l);
-                __stcg(st.lse_part + (int64_t)J.slot * kUnitRows + prow, lse_own);
-                __threadfence();
-                *reinterpret_cast<volatile uint32_t*>(st.piece_flag + (int64_t)J.slot * kUnitRows + prow) = epoch;
+                    for (int c = 0; c < D; ++c) __stcg(ocol + (int64_t)c * kUnitRows, __uint_as_float(ov[c]) * inv_l);
+                    __stcg(st.lse_part + (int64_t)J.slot * kUnitRows + prow, lse_own);
+                    __threadfence();
+                    *reinterpret_cast<volatile uint32_t*>(st.piece_flag + (int64_t)J.slot * kUnitRows + prow) = 1u;
+                }
                 continue;
             }
             // the first key range merges: the other pieces of the unit (finished earlier,
@@ -693,7 +708,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
             bool have = true;
             if (live)
                 for (int pp = 1; pp <= n_other && have; ++pp)
-                    have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, epoch, wt);
+                    have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, 1u, wt);
             if (__any_sync(0xffffffffu, !have)) { ok = false; break; }
             __threadfence();
             // ---- beam scores q . k_j / sqrt(D)
@@ -783,6 +798,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, int 
 #pragma unroll
                     for (int u = 0; u < 32; ++u) a[c0 + u] = fmaf(w, x[u], a[c0 + u]);
                 }
+                st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
             }
             // ---- BeamKV values
             for (int j = 0; j < t; ++j) {
@@ -867,9 +883,8 @@ cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes) {
 }
 
 template <int D>
-cudaError_t launch_ctx_attn_d(const GrState& st, const CUtensorMap& qmap, int layer, int t, const uint16_t* q,
-                              uint16_t* out, uint32_t epoch, float scale_log2, float scale, int64_t wait_limit_ns,
-                              cudaStream_t s) {
+cudaError_t launch_ctx_attn_d(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
+                              uint16_t* out, float scale_log2, float scale, int64_t wait_limit_ns, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_ctx_attn<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -889,18 +904,15 @@ cudaError_t launch_ctx_attn_d(const GrState& st, const CUtensorMap& qmap, int la
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_ctx_attn<D>, qmap, st, layer, t, q, out, epoch, scale_log2, scale,
-                              wait_limit_ns);
+    return cudaLaunchKernelEx(&cfg, k_ctx_attn<D>, qmap, st, layer, q, out, scale_log2, scale, wait_limit_ns);
 }
 
-cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, int t, const uint16_t* q,
-                            uint16_t* out, uint32_t epoch, int64_t wait_limit_ns, cudaStream_t s) {
+cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
+                            uint16_t* out, int64_t wait_limit_ns, cudaStream_t s) {
     const float scale = 1.f / sqrtf((float)st.head_dim);
     const float scale_log2 = scale * 1.4426950408889634f;
-    if (st.head_dim == 128)
-        return launch_ctx_attn_d<128>(st, qmap, layer, t, q, out, epoch, scale_log2, scale, wait_limit_ns, s);
-    if (st.head_dim == 64)
-        return launch_ctx_attn_d<64>(st, qmap, layer, t, q, out, epoch, scale_log2, scale, wait_limit_ns, s);
+    if (st.head_dim == 128) return launch_ctx_attn_d<128>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
+    if (st.head_dim == 64) return launch_ctx_attn_d<64>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
     return cudaErrorInvalidValue;
 }
 

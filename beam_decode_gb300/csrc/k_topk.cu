@@ -55,10 +55,13 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
     }
 }
 
-__device__ __forceinline__ bool row_live(const GrState& st, int row, int t, int& r, int& b) {
+// a row takes part in the step when its request is still decoding (t_r < L_r) and the
+// row holds one of the request's live beams
+__device__ __forceinline__ bool row_live(const GrState& st, int row, int& r, int& b, int& t) {
     r = st.row_req[row];
     const GrReqDev& R = st.req[r];
     b = row - R.row_off;
+    t = st.req_step[r];
     if (t >= R.n_levels) return false;
     return b < st.n_beams[r * (st.n_levels + 1) + t];
 }
@@ -69,14 +72,15 @@ __device__ __forceinline__ bool row_live(const GrState& st, int row, int t, int&
 constexpr int kLsThreads = 256;
 
 __global__ void __cluster_dims__(kLogitCluster, 1, 1) __launch_bounds__(kLsThreads)
-k_logsoftmax_gather(GrState st, int t, const float* __restrict__ logits, int64_t ld,
+k_logsoftmax_gather(GrState st, const float* __restrict__ logits, int64_t ld,
                     float* __restrict__ logprobs_out, float* __restrict__ lse_out,
                     const float* __restrict__ lse_in) {
     cg::cluster_group cluster = cg::this_cluster();
     const int row = blockIdx.x / kLogitCluster;
     const int part = (int)cluster.block_rank();
     int r, b;
-    if (!row_live(st, row, t, r, b)) return;  // uniform over the cluster
+    int t;
+    if (!row_live(st, row, r, b, t)) return;  // uniform over the cluster
 
     __shared__ float red_m[kLsThreads / 32], red_s[kLsThreads / 32];
     __shared__ float part_ms[2];
@@ -321,11 +325,12 @@ __device__ void select_global(SelSmem& sm, const uint32_t* keys, int N, uint32_t
     (void)k_want;
 }
 
-__global__ void __launch_bounds__(kSelThreads) k_topk_select(GrState st, int t) {
+__global__ void __launch_bounds__(kSelThreads) k_topk_select(GrState st) {
     extern __shared__ __align__(16) uint8_t sel_smem_raw[];
     SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_smem_raw);
     const int r = blockIdx.x;
     const GrReqDev R = st.req[r];
+    const int t = st.req_step[r];
     if (t >= R.n_levels) return;
     const int C = st.C;
     const int n_live = st.n_beams[r * (st.n_levels + 1) + t];
@@ -477,13 +482,20 @@ __global__ void __launch_bounds__(kSelThreads) k_topk_select(GrState st, int t) 
 // ---------------------------------------------------------------------------
 // K5: BeamPath advance (no KV copies)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kMaxBeam) k_advance(GrState st, int t) {
+__global__ void __launch_bounds__(kMaxBeam) k_advance(GrState st) {
     const int r = blockIdx.x;
     const GrReqDev R = st.req[r];
+    __shared__ int t_sh;
+    if (threadIdx.x == 0) t_sh = st.req_step[r];
+    __syncthreads();
+    const int t = t_sh;
     if (t >= R.n_levels) return;
     const int L = st.n_levels;
     const int n = st.n_sel[r];
-    if (threadIdx.x == 0) st.n_beams[r * (L + 1) + t + 1] = n;
+    if (threadIdx.x == 0) {
+        st.n_beams[r * (L + 1) + t + 1] = n;
+        st.req_step[r] = t + 1;  // every thread has its copy of t already
+    }
     const int i = threadIdx.x;
     if (i >= n) return;
     const int row = R.row_off + i;
@@ -536,7 +548,21 @@ __global__ void k_init_state(GrState st) {
     const int L1 = st.n_levels + 1;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < st.n_req * L1; i += gridDim.x * blockDim.x)
         st.n_beams[i] = (i % L1 == 0) ? 1 : 0;
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < st.n_req; r += gridDim.x * blockDim.x) st.req_step[r] = 0;
     if (blockIdx.x == 0 && threadIdx.x < 4) st.status[threadIdx.x] = 0;
+}
+
+// a request (re)starts at level 0 with its single root beam
+__global__ void k_init_request(GrState st, int r) {
+    const int L1 = st.n_levels + 1;
+    for (int i = threadIdx.x; i < L1; i += blockDim.x) st.n_beams[r * L1 + i] = (i == 0) ? 1 : 0;
+    if (threadIdx.x == 0) st.req_step[r] = 0;
+}
+
+// every request past `step` goes back to it (its levels 0..step-1 stay committed)
+__global__ void k_set_step(GrState st, int step) {
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < st.n_req; r += gridDim.x * blockDim.x)
+        if (st.req_step[r] > step) st.req_step[r] = step;
 }
 
 }  // namespace
@@ -546,15 +572,25 @@ cudaError_t launch_init_state(const GrState& st, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_logsoftmax_gather(const GrState& st, int t, const float* logits, int64_t ld,
-                                     float* logprobs_out, float* lse_out, const float* lse_in,
-                                     cudaStream_t s) {
-    dim3 grid(st.rows * kLogitCluster);
-    k_logsoftmax_gather<<<grid, kLsThreads, 0, s>>>(st, t, logits, ld, logprobs_out, lse_out, lse_in);
+cudaError_t launch_init_request(const GrState& st, int r, cudaStream_t s) {
+    k_init_request<<<1, 32, 0, s>>>(st, r);
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk_select(const GrState& st, int t, cudaStream_t s) {
+cudaError_t launch_set_step(const GrState& st, int step, cudaStream_t s) {
+    k_set_step<<<1, 256, 0, s>>>(st, step);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_logsoftmax_gather(const GrState& st, const float* logits, int64_t ld,
+                                     float* logprobs_out, float* lse_out, const float* lse_in,
+                                     cudaStream_t s) {
+    dim3 grid(st.rows * kLogitCluster);
+    k_logsoftmax_gather<<<grid, kLsThreads, 0, s>>>(st, logits, ld, logprobs_out, lse_out, lse_in);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk_select(const GrState& st, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -562,12 +598,12 @@ cudaError_t launch_topk_select(const GrState& st, int t, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    k_topk_select<<<st.n_req, kSelThreads, sizeof(SelSmem), s>>>(st, t);
+    k_topk_select<<<st.n_req, kSelThreads, sizeof(SelSmem), s>>>(st);
     return cudaGetLastError();
 }
 
-cudaError_t launch_advance(const GrState& st, int t, cudaStream_t s) {
-    k_advance<<<st.n_req, kMaxBeam, 0, s>>>(st, t);
+cudaError_t launch_advance(const GrState& st, cudaStream_t s) {
+    k_advance<<<st.n_req, kMaxBeam, 0, s>>>(st);
     return cudaGetLastError();
 }
 

@@ -15,13 +15,27 @@
  * TensorRT LLM", section "Background: what inference a recommendation request
  * needs").
  *
- * One step t (t = 0 .. L-1, L = semantic-ID length) is, in call order:
- *   [t >= 1] for every layer: the caller writes the K/V of the token chosen at
- *            level t-1 into gr_beam_kv_slot(), then calls gr_decode_attn();
- *   gr_constrained_topk() on the step's logit rows (for t = 0: the prefill
- *            logits, one live row per request);
- *   gr_beam_advance().
- * After step L-1, gr_beam_results() returns all beams of a request.
+ * Each request r decodes its own step t_r = 0 .. L_r-1 (L_r = the semantic-ID
+ * length of its catalogue, at most gr_config.n_levels).  One batch step is, in
+ * call order:
+ *   for every layer: the caller writes the K/V of the token each request with
+ *            t_r >= 1 chose at level t_r-1 into its BeamKV slot
+ *            (gr_beam_kv_slot_request / gr_beam_kv_slot), then calls
+ *            gr_decode_attn();
+ *   gr_constrained_topk() on the step's logit rows (for a request at t_r = 0:
+ *            its prefill logits, one live row);
+ *   gr_beam_advance(), which moves every request that is still decoding to
+ *            t_r + 1.
+ * Requests therefore need not be in step: requests of different lengths share
+ * a batch, and a finished request's slot can take a new request
+ * (gr_beam_admit) while the others keep decoding (GR-native continuous
+ * batching, same article and section).  When t_r reaches L_r,
+ * gr_beam_results() returns all beams of request r.
+ *
+ * The step state lives on the device (every kernel reads t_r there and
+ * gr_beam_advance moves it), so a whole captured step replays as a CUDA graph
+ * without the host (direct-pool-view CUDA-graph replay, same section): see
+ * gr_beam_set_graph_mode.
  *
  * Conventions
  *   - Memory: the caller allocates and owns every device buffer (ContextKV
@@ -87,7 +101,8 @@ typedef struct {
     int64_t ctx_offset;    /* first token of this request in the ContextKV pool */
     int ctx_len;           /* T_r >= 1; ctx_offset + T_r <= pool_tokens         */
     int beam_width;        /* W_r: maximum beams, 1..1024                       */
-    const gr_trie* trie;   /* catalogue; its n_levels / C must match gr_config  */
+    const gr_trie* trie;   /* catalogue: C must match gr_config, its n_levels   */
+                           /* (= L_r) may be 1..gr_config.n_levels              */
 } gr_request;
 
 /* Device buffers of a batch (all owned by the caller). */
@@ -146,24 +161,34 @@ gr_status gr_beam_destroy(gr_beam* beam);
 /* rows_total = sum of W_r; row_offsets (optional, n_requests+1 ints) gets the
  * first row of each request and rows_total last. */
 gr_status gr_beam_rows(const gr_beam* beam, int* rows_total, int* row_offsets);
-/* Current step t (0..L; L means decoding is finished). */
+/* Batch steps (gr_beam_advance calls) since create or the last rewind; for a
+ * batch whose requests started together this is every request's t_r. */
 gr_status gr_beam_step(const gr_beam* beam, int* step);
+/* Step t_r of one request (t_r == L_r: finished) and its length L_r; either
+ * output may be NULL.  After graph-mode replays call gr_beam_sync first. */
+gr_status gr_beam_request_step(const gr_beam* beam, int request, int* step, int* n_levels);
 
-/* Zero-copy view of BeamKV for the token chosen at level t-1 (t = current
- * step >= 1): bf16 [rows][n_kv_heads][head_dim] for `layer`.  The caller writes
+/* Zero-copy view of BeamKV for the token chosen at level t-1, when every
+ * request with a BeamKV level open is at the same step t >= 1 (GR_ERR_STATE
+ * otherwise): bf16 [rows][n_kv_heads][head_dim] for `layer`.  The caller writes
  * each live beam's new K and V there (slot b = row b) before gr_decode_attn. */
 gr_status gr_beam_kv_slot(gr_beam* beam, int layer, void** k_new, void** v_new);
+/* The same view for one request at its own step t_r >= 1: bf16
+ * [W_r][n_kv_heads][head_dim] (rows row_off[r] ..), level t_r-1 of `layer`. */
+gr_status gr_beam_kv_slot_request(gr_beam* beam, int layer, int request, void** k_new, void** v_new);
 
 /* ------------------------------------------------------------------------ */
 /* Hot path                                                                  */
 /* ------------------------------------------------------------------------ */
 
-/* GQA decode attention of every live beam at the current step t >= 1, layer
- * `layer`: beam b of request r attends to its request's T_r context tokens
- * followed by the t BeamKV tokens on its path (levels 0..t-1, slots from
- * BeamPath), scale 1/sqrt(D).
+/* GQA decode attention, layer `layer`, of every live beam of every request at
+ * a step 1 <= t_r < L_r: beam b of request r attends to its request's T_r
+ * context tokens followed by the t_r BeamKV tokens on its path (levels
+ * 0..t_r-1, slots from BeamPath), scale 1/sqrt(D).
  *   q   bf16 [rows][n_q_heads][head_dim], 16-byte aligned
- *   out bf16 [rows][n_q_heads][head_dim]; dead rows are written as zeros
+ *   out bf16 [rows][n_q_heads][head_dim]; rows of dead beams of those requests
+ *       are written as zeros, rows of other requests (t_r == 0 or finished)
+ *       are not written
  * The context part runs on the tensor cores (tcgen05, TMA-fed, every context
  * byte read once per request), the BeamKV part with vector loads, merged by
  * a log-sum-exp combine.  Each layer may be called once per step. */
@@ -186,19 +211,41 @@ gr_status gr_decode_attn(gr_beam* beam, int layer, const void* q, void* out, gr_
 gr_status gr_constrained_topk(gr_beam* beam, const float* logits, int64_t ld, float* logprobs_out,
                               float* lse_out, const float* lse_in, gr_stream_t stream);
 
-/* Commit the selection of step t to BeamPath (parent slot, token, trie node,
- * score, ancestry) and set the live width of step t+1; no KV is moved.  The
- * step counter becomes t+1. */
+/* Commit each decoding request's selection of its step t_r to BeamPath
+ * (parent slot, token, trie node, score, ancestry) and set the live width of
+ * step t_r+1; no KV is moved.  Every decoding request moves to t_r+1. */
 gr_status gr_beam_advance(gr_beam* beam, gr_stream_t stream);
 
-/* Set the step counter back to `step` (0 <= step <= current step) so that
- * step `step` can be decoded again from the BeamPath levels before it (host
- * state only; nothing is enqueued).  Step 0 starts again from the root beam. */
-gr_status gr_beam_rewind(gr_beam* beam, int step);
+/* Every request past step `step` goes back to it, so that it can be decoded
+ * again from the BeamPath levels before it; step 0 starts again from the root
+ * beam.  0 <= step <= gr_beam_step() (GR_ERR_STATE otherwise; not checked in
+ * graph mode).  Enqueued on `stream` (one kernel and nothing else, so it can be
+ * part of a captured graph). */
+gr_status gr_beam_rewind(gr_beam* beam, int step, gr_stream_t stream);
 
-/* All surviving beams of request `request` after the last step, best first
- * (synchronises `stream`):
- *   codes     int32 [W_r][n_levels]   code of each level
+/* GR-native continuous batching: slot `request` (finished, t_r == L_r, or not
+ * started, t_r == 0) takes a new request between two batch steps.  Its
+ * beam_width must fit the slot's rows (the slot's W_r at create); context
+ * and catalogue are free.  The attention schedule is rebuilt on the host and
+ * its tables (a few KB) are copied into the workspace on `stream`, after the
+ * work already queued there; the new request starts at t_r = 0 with one root
+ * beam.  GR_ERR_STATE in the middle of a step or in graph mode. */
+gr_status gr_beam_admit(gr_beam* beam, int request, const gr_request* req, gr_stream_t stream);
+
+/* Graph mode (enable != 0, between steps): gr_decode_attn, gr_constrained_topk,
+ * gr_beam_advance and gr_beam_rewind only enqueue their kernels, taking every
+ * decision from the device-resident step state, so the calls of a step can be
+ * captured once (cudaStreamBeginCapture or a framework's graph capture) and
+ * the graph replayed for later steps.  The host's copy of the step state is
+ * not updated meanwhile: gr_beam_sync reloads it.  Timing events are off. */
+gr_status gr_beam_set_graph_mode(gr_beam* beam, int enable);
+/* Reload the host's copy of every request's step from the device (synchronises
+ * `stream`) and report the device status word. */
+gr_status gr_beam_sync(gr_beam* beam, gr_stream_t stream);
+
+/* All surviving beams of request `request` once it finished (t_r == L_r),
+ * best first (synchronises `stream`):
+ *   codes     int32 [W_r][L_r]        code of each level
  *   item_ids  int64 [W_r]             item of the code string
  *   scores    fp32  [W_r]             sum of the code log-probabilities
  *   n_out     number of beams written

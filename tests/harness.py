@@ -230,3 +230,162 @@ class LockStep:
 
     def gpu_results(self, r: int):
         return self.beam.results(r)
+
+
+@dataclasses.dataclass
+class Occupant:
+    """One request that holds a batch slot for a while (continuous batching)."""
+    ctx_len: int
+    width: int
+    n_levels: int
+    n_items: int
+    key: int                 # seeds its catalogue and BeamKV streams
+
+
+class MixedDriver:
+    """Requests at their own steps: each slot holds one occupant (context, catalogue,
+    length L_r, width); the batch advances with one call sequence per batch step while
+    the occupants are at different levels, and a finished slot takes the next occupant
+    (gr_beam_admit).  The GPU batch and one oracle beam per occupant see the same
+    host-generated inputs; every comparison is against the oracle."""
+
+    def __init__(self, occupants: List[Occupant], slot_widths: List[int], n_layers=2, n_q_heads=4, n_kv_heads=2,
+                 head_dim=64, vocab=2048, codes_per_level=32, n_levels_max=3, seed=50, device="cuda"):
+        import torch
+        from beam_decode_gb300 import binding as B
+        self.torch, self.B, self.device = torch, B, device
+        self.NL, self.Hq, self.Hkv, self.D = n_layers, n_q_heads, n_kv_heads, head_dim
+        self.V, self.C, self.Lmax, self.seed = vocab, codes_per_level, n_levels_max, seed
+        self.code_base = vocab - n_levels_max * codes_per_level
+        self.occ = list(occupants)
+        # ContextKV pool: one region per occupant, gaps between them
+        self.ctx_off, off = [], 5
+        for o in self.occ:
+            self.ctx_off.append(off)
+            off += o.ctx_len + 9
+        shp = (n_layers, n_kv_heads, off, head_dim)
+        self.ctx_k = wl.round_to_bf16(wl.host_normal(shp, seed, wl.TAG_CTX_K))
+        self.ctx_v = wl.round_to_bf16(wl.host_normal(shp, seed, wl.TAG_CTX_V))
+        tk = torch.from_numpy(self.ctx_k).to(torch.bfloat16).to(device)
+        tv = torch.from_numpy(self.ctx_v).to(torch.bfloat16).to(device)
+        self.items = [wl.draw_items(o.n_items, o.n_levels, codes_per_level, "uniform", seed, stream=(o.key,))
+                      for o in self.occ]
+        self.gtries = [B.Trie(it, codes_per_level=codes_per_level, device=device) for it in self.items]
+        self.otries = [OTrie(it, codes_per_level=codes_per_level) for it in self.items]
+        self.slot_w = list(slot_widths)
+        self.slot_occ = list(range(len(slot_widths)))   # occupant held by each slot
+        reqs = [(self.ctx_off[i], self.occ[i].ctx_len, self.occ[i].width, self.gtries[i])
+                for i in range(len(slot_widths))]
+        # slots are created at their full widths (rows); the first occupants use them all
+        assert all(self.occ[i].width == slot_widths[i] for i in range(len(slot_widths)))
+        self.beam = B.Beam(n_layers, n_q_heads, n_kv_heads, head_dim, vocab, self.code_base, n_levels_max,
+                           codes_per_level, tk, tv, reqs, device=device)
+        self.row_off = self.beam.row_offsets
+        self.rows = self.beam.rows
+        self.obeam = {i: self._oracle(i) for i in range(len(slot_widths))}
+        self.obk: Dict[int, Dict] = {}   # occupant -> {(layer, level): (k, v)}
+        self.k = 0                       # batch steps so far
+        self.finished: List[int] = []
+
+    def _oracle(self, o):
+        return OracleBeam(self.otries[o], self.occ[o].width, self.occ[o].n_levels, self.C, self.code_base,
+                          key_mode="f32")
+
+    def t(self, slot):
+        return self.obeam[self.slot_occ[slot]].t
+
+    def L(self, slot):
+        return self.occ[self.slot_occ[slot]].n_levels
+
+    def admit(self, slot, o):
+        oc = self.occ[o]
+        self.beam.admit(slot, self.ctx_off[o], oc.ctx_len, oc.width, self.gtries[o])
+        self.slot_occ[slot] = o
+        self.obeam[o] = self._oracle(o)
+
+    def step(self, compare=True) -> Dict:
+        torch = self.torch
+        S = len(self.slot_w)
+        attending = [s for s in range(S) if 1 <= self.t(s) < self.L(s)]
+        decoding = [s for s in range(S) if self.t(s) < self.L(s)]
+        worst = 0.0
+        if attending:
+            for layer in range(self.NL):
+                for s in attending:
+                    o, t = self.slot_occ[s], self.t(s)
+                    shp = (self.slot_w[s], self.Hkv, self.D)
+                    kk = wl.round_to_bf16(wl.host_normal(shp, self.seed, wl.TAG_BEAM_K, sub=(1000 + o, t - 1, layer)))
+                    vv = wl.round_to_bf16(wl.host_normal(shp, self.seed, wl.TAG_BEAM_V, sub=(1000 + o, t - 1, layer)))
+                    gk, gv = self.beam.kv_slot(layer, request=s)
+                    gk.copy_(torch.from_numpy(kk).to(torch.bfloat16))
+                    gv.copy_(torch.from_numpy(vv).to(torch.bfloat16))
+                    self.obk.setdefault(o, {})[(layer, t - 1)] = (kk, vv)
+                q = wl.round_to_bf16(wl.host_normal((self.rows, self.Hq, self.D), self.seed, wl.TAG_Q,
+                                                    sub=(self.k, layer)))
+                gq = torch.from_numpy(q).to(torch.bfloat16).to(self.device)
+                gout = torch.full_like(gq, float("nan"))
+                self.beam.decode_attn(layer, gq, gout)
+                if not compare:
+                    continue
+                out = gout.float().cpu().numpy()
+                for s in range(S):
+                    r0, W = self.row_off[s], self.slot_w[s]
+                    if s not in attending:  # rows of requests that do not attend are not written
+                        if not np.all(np.isnan(out[r0:r0 + W])):
+                            worst = float("inf")
+                        continue
+                    o, t = self.slot_occ[s], self.t(s)
+                    ob = self.obeam[o]
+                    n_live = ob.n_live()
+                    T, c0 = self.occ[o].ctx_len, self.ctx_off[o]
+                    bk = [self.obk[o][(layer, j)][0] for j in range(t)]
+                    bv = [self.obk[o][(layer, j)][1] for j in range(t)]
+                    ref = beam_attention(q[r0:r0 + W], self.ctx_k[layer, :, c0:c0 + T], self.ctx_v[layer, :, c0:c0 + T],
+                                         bk, bv, ob.ancestry(), beams=list(range(n_live)))
+                    got = out[r0:r0 + n_live]
+                    viol = np.abs(got - ref) / (ATOL + RTOL * np.abs(ref))
+                    worst = max(worst, float(np.max(viol)) if viol.size else 0.0)
+                    # dead beams of the request are zeros; slot rows past its width are not written
+                    w_occ = self.occ[o].width
+                    if np.isnan(got).any() or not np.all(out[r0 + n_live:r0 + w_occ] == 0):
+                        worst = float("inf")
+        # top-K of every decoding request at its own level
+        from oracle import log_softmax_row
+        x = wl.host_normal((self.rows, self.V), self.seed, wl.TAG_LOGITS, sub=(self.k,), std=2.0)
+        lse32 = np.zeros(self.rows, dtype=np.float32)
+        for s in decoding:
+            o, r0 = self.slot_occ[s], self.row_off[s]
+            n = self.obeam[o].n_live()
+            rows = x[r0:r0 + n]
+            lse32[r0:r0 + n] = np.array([log_softmax_row(rw)[1] for rw in rows], dtype=np.float32)
+            self.obeam[o].step(rows, lse_in=lse32[r0:r0 + n])
+        self.beam.constrained_topk(torch.from_numpy(x).to(self.device),
+                                   lse_in=torch.from_numpy(lse32).to(self.device))
+        self.beam.advance()
+        mismatch = []
+        for s in decoding:
+            o = self.slot_occ[s]
+            ob = self.obeam[o]
+            t = ob.t - 1
+            par, tok, _, sc = self.beam.path(s, t)
+            exp_tok = np.array([self.code_base + t * self.C + c for c in ob.codes[t]], dtype=np.int32)
+            exp_sc = np.array([float(v) for v in ob.scores[t]], dtype=np.float32)
+            if not (np.array_equal(par, np.array(ob.parents[t], dtype=np.int32)) and np.array_equal(tok, exp_tok)
+                    and np.array_equal(sc.view(np.uint32), exp_sc.view(np.uint32))):
+                mismatch.append((s, o, t))
+            assert self.beam.request_step(s) == (ob.t, self.occ[o].n_levels)
+            if ob.t == self.occ[o].n_levels:
+                self.check_results(s)
+                self.finished.append(o)
+        self.k += 1
+        return {"worst": worst, "mismatch": mismatch, "attending": attending, "decoding": decoding}
+
+    def check_results(self, s):
+        o = self.slot_occ[s]
+        codes, items, scores = self.beam.results(s)
+        exp = self.obeam[o].results()
+        assert len(codes) == len(exp), (s, o)
+        for i, (tup, iid, sc) in enumerate(exp):
+            assert tuple(int(c) for c in codes[i]) == tup
+            assert int(items[i]) == iid
+            assert np.float32(scores[i]).view(np.uint32) == np.float32(sc).view(np.uint32)

@@ -115,7 +115,7 @@ def test_workspace_bytes_rejects_requests(lib):
 
 def test_null_handles(lib):
     assert lib.gr_beam_advance(None, None) == B.GR_ERR_INVALID_ARG
-    assert lib.gr_beam_rewind(None, 1) == B.GR_ERR_INVALID_ARG
+    assert lib.gr_beam_rewind(None, 1, None) == B.GR_ERR_INVALID_ARG
     assert lib.gr_decode_attn(None, 0, None, None, None) == B.GR_ERR_INVALID_ARG
     assert lib.gr_constrained_topk(None, None, 0, None, None, None, None) == B.GR_ERR_INVALID_ARG
     n = ctypes.c_int()
