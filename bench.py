@@ -131,6 +131,27 @@ class DeviceBatch:
         b.constrained_topk(self.logits[1])
         b.advance()
 
+    def capture(self):
+        """Record the step once as a CUDA graph (graph mode: every decision inside comes from
+        the device-resident step state); returns the library launches one replay makes."""
+        torch = self.torch
+        from beam_decode_gb300 import binding as B
+        self.step()  # outside the capture: one-time kernel attribute setup
+        torch.cuda.synchronize()
+        for k in range(B.KERNEL_KINDS):
+            self.beam.kernel_stats(k, reset=True)
+        self.beam.set_graph_mode(True)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.step()
+        return sum(self.beam.kernel_stats(k, reset=True)[0] for k in range(B.KERNEL_KINDS))
+
+    def release(self):
+        """Leave graph mode and reload the host's step state."""
+        self.graph = None
+        self.beam.set_graph_mode(False)
+        self.beam.sync()
+
     # algorithmic work of one step
     def attn_flops(self) -> float:
         w = self.w
@@ -279,31 +300,46 @@ def run_gpu(args, w):
     if beam.status() != 0:
         raise RuntimeError("device status error during warm-up")
 
+    def timed(run_step, sample_clocks):
+        clocks = Clocks(local) if sample_clocks else None
+        if clocks:
+            time.sleep(0.3)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            run_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        ck = clocks.stop() if clocks else None
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, ck
+
+    # eager launches, each bracketed by CUDA events on its stream: the per-kernel split
     for k in range(B.KERNEL_KINDS):
         beam.kernel_stats(k, reset=True)
     beam.set_timing(True)
-    clocks = Clocks(local)
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        batch.step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    ck = clocks.stop()
+    ms_eager, ck = timed(batch.step, args.no_graph)  # clocks here only when this is the headline
     beam.set_timing(False)
     stats = {B.KERNEL_NAMES[k]: beam.kernel_stats(k, reset=True) for k in range(B.KERNEL_KINDS)}
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = ms_eager
+    launches = sum(n for (n, _) in stats.values())
+    if not args.no_graph:
+        # the headline: the same step captured once and replayed as a CUDA graph
+        per_step = batch.capture()
+        for _ in range(args.warmup):
+            batch.graph.replay()
+        ms, ck = timed(batch.graph.replay, True)
+        launches = per_step * args.steps
+        batch.release()
     ms_per_step = ms / args.steps
     value = world * 1000.0 / ms_per_step
-    launches = sum(n for (n, _) in stats.values())
     st = beam.status()
     if st != 0:
         raise RuntimeError(f"device status error {st}")
@@ -343,7 +379,10 @@ def run_gpu(args, w):
                            "beam": w.beam_widths[0], "layers": w.n_layers, "q_heads": w.n_q_heads,
                            "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "vocab": w.vocab,
                            "levels": w.n_levels, "codes": w.codes_per_level, "items": w.n_items[0],
-                           "l2": "inputs larger than L2 (ContextKV 4.6 GB)", "parallelism": f"replicas{world}"},
+                           "l2": "inputs larger than L2 (ContextKV 4.6 GB)", "parallelism": f"replicas{world}",
+                           "cuda_graph": not args.no_graph},
+                "eager": {"value": world * 1000.0 / (ms_eager / args.steps), "unit": "steps/s",
+                          "ms_per_step": ms_eager / args.steps},
                 "roofline": roofline,
                 "hbm_kernels": hbm,
                 "kernels": per_kernel,
@@ -413,6 +452,7 @@ def main():
     ap.add_argument("--impl", default="gr", choices=["gr", "reference"])
     ap.add_argument("--workload", default="long", choices=["tiny", "page1", "short", "long", "mixed"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a replayed CUDA graph")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests of the workload (a smaller case for profiling)")
     args = ap.parse_args()
