@@ -399,11 +399,14 @@ def run_gpu(args, w):
 
 
 def run_e2e(args, batch: DeviceBatch):
-    """Same step through the public API with pinned host inputs copied in and
-    the step's selection read back every step."""
+    """Same step through the public API with pinned host inputs copied in and the
+    step's selection read back every step.  The copies run on their own stream,
+    layer by layer, so that a layer's inputs arrive while earlier layers compute;
+    events keep every device buffer from being overwritten before its consumer ran."""
     import torch
     w = batch.w
     beam = batch.beam
+    NL = w.n_layers
     host_q = [q.cpu().pin_memory() for q in batch.q]
     host_k = [k.cpu().pin_memory() for k in batch.new_k]
     host_v = [v.cpu().pin_memory() for v in batch.new_v]
@@ -411,22 +414,39 @@ def run_e2e(args, batch: DeviceBatch):
     dq = [torch.empty_like(q) for q in batch.q]
     dx = torch.empty_like(batch.logits[1])
     h2d = sum(t.numel() * t.element_size() for t in host_q + host_k + host_v) + host_x.numel() * 4
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    arrived = [torch.cuda.Event() for _ in range(NL + 1)]   # inputs of layer l (NL: logits) on the device
+    used = [torch.cuda.Event() for _ in range(NL + 1)]      # the step's consumer of those buffers ran
+    for e in used:
+        e.record(comp)
+    # BeamKV slots of level 0 (the open level at step 1) for every layer
+    kv = [beam.kv_slot(l) for l in range(NL)]
     d2h = 0
 
     def one():
         nonlocal d2h
+        with torch.cuda.stream(copy):
+            for l in range(NL):
+                copy.wait_event(used[l])
+                kv[l][0].copy_(host_k[l], non_blocking=True)
+                kv[l][1].copy_(host_v[l], non_blocking=True)
+                dq[l].copy_(host_q[l], non_blocking=True)
+                arrived[l].record(copy)
+            copy.wait_event(used[NL])
+            dx.copy_(host_x, non_blocking=True)
+            arrived[NL].record(copy)
         beam.rewind(1)
-        for l in range(w.n_layers):
-            k, v = beam.kv_slot(l)
-            k.copy_(host_k[l], non_blocking=True)
-            v.copy_(host_v[l], non_blocking=True)
-            dq[l].copy_(host_q[l], non_blocking=True)
+        for l in range(NL):
+            comp.wait_event(arrived[l])
             beam.decode_attn(l, dq[l], batch.out[l])
-        dx.copy_(host_x, non_blocking=True)
+            used[l].record(comp)
+        comp.wait_event(arrived[NL])
         beam.constrained_topk(dx)
+        used[NL].record(comp)
         beam.advance()
         n = 0
-        for r in range(w.n_requests):
+        for r in range(w.n_requests):  # the step's selection, read back (synchronises)
             par, tok, nod, sc = beam.path(r, 1)
             n += (par.nbytes + tok.nbytes + sc.nbytes)
         d2h = n
@@ -440,8 +460,13 @@ def run_e2e(args, batch: DeviceBatch):
         one()
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
+    # the host->device copy rate alone, for reading the number
+    t1 = time.perf_counter()
+    dx.copy_(host_x, non_blocking=True)
+    torch.cuda.synchronize()
+    gbs = host_x.numel() * 4 / (time.perf_counter() - t1) / 1e9
     return {"value": 1.0 / dt, "unit": "steps/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": steps}
+            "steps": steps, "h2d_GB_s_single_copy": gbs}
 
 
 def main():
