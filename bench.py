@@ -273,6 +273,31 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------------------
+# replicas (N > 1): the path shards by request, so ranks decode independent
+# batches and only the timing is reduced
+# ---------------------------------------------------------------------------
+def replica_workload(w, rank: int):
+    """Each rank decodes its own batch of the same shape, seeded apart."""
+    return w if rank == 0 else wl.make_workload(w.name, seed=w.seed + 1000 * rank)
+
+
+def job_time_ms(ms_local: float, world: int, device) -> float:
+    """The job's time is the slowest replica's: all-reduce MAX over the ranks."""
+    if world == 1:
+        return ms_local
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every replica completes one step per ms_per_step."""
+    return world * 1000.0 / ms_per_step
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def run_gpu(args, w):
@@ -287,9 +312,7 @@ def run_gpu(args, w):
     if world > 1:
         dist.init_process_group("nccl")
     dev = f"cuda:{local}"
-    # replicas only: each rank decodes its own batch (seed offset by rank)
-    if rank:
-        w = wl.make_workload(w.name, seed=w.seed + 1000 * rank)
+    w = replica_workload(w, rank)
     batch = DeviceBatch(w, dev)
     beam = batch.beam
     stream = torch.cuda.current_stream()
@@ -315,11 +338,7 @@ def run_gpu(args, w):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
         ck = clocks.stop() if clocks else None
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms, ck
+        return job_time_ms(ms, world, dev), ck
 
     # eager launches, each bracketed by CUDA events on its stream: the per-kernel split
     for k in range(B.KERNEL_KINDS):
@@ -339,7 +358,7 @@ def run_gpu(args, w):
         launches = per_step * args.steps
         batch.release()
     ms_per_step = ms / args.steps
-    value = world * 1000.0 / ms_per_step
+    value = job_value(ms_per_step, world)
     st = beam.status()
     if st != 0:
         raise RuntimeError(f"device status error {st}")
@@ -381,7 +400,7 @@ def run_gpu(args, w):
                            "levels": w.n_levels, "codes": w.codes_per_level, "items": w.n_items[0],
                            "l2": "inputs larger than L2 (ContextKV 4.6 GB)", "parallelism": f"replicas{world}",
                            "cuda_graph": not args.no_graph},
-                "eager": {"value": world * 1000.0 / (ms_eager / args.steps), "unit": "steps/s",
+                "eager": {"value": job_value(ms_eager / args.steps, world), "unit": "steps/s",
                           "ms_per_step": ms_eager / args.steps},
                 "roofline": roofline,
                 "hbm_kernels": hbm,
