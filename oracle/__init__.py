@@ -17,6 +17,10 @@ step below is the plainest reading of their prose):
       time; beam search keeps the highest-scoring prefixes, expands and
       prunes them at each step, and returns every surviving beam, not only
       the best one.
+    - section "Scoring many candidates at once": multi-item scoring -- user
+      prefix and every candidate in one sequence, a mask that lets each
+      candidate see only the prefix and itself, label-token log-probabilities
+      read out, candidates ranked by them.
 [RECSYS] zhiding.cn article on NVIDIA recsys-examples and nv-embedding-cache.
     - section "语义ID：解决稀疏性与长尾问题" (semantic IDs): decoding semantic
       IDs yields the recommendation directly, and the output logits give the
@@ -31,6 +35,8 @@ Modules:
     attention    -- per-beam attention over the concatenated context+beam sequence
     beam_search  -- full-vocabulary log-softmax, constrained candidate
                     enumeration, sort-based selection, beam state and results
+    scoring      -- multi-item scoring: masked attention of candidate tokens,
+                    label-token log-probabilities, ranking
 
 Parity pins: see tests/test_oracle_*.py.  Every function here is pinned by a
 library routine, a closed form, brute-force enumeration, an invariant, or a
@@ -40,6 +46,8 @@ from .trie import Trie
 from .attention import attend_row, beam_attention
 from .beam_search import (log_softmax_row, OracleBeam, exhaustive_scores, token_id,
                           key_f32, ordered_f32)
+from .scoring import label_logprobs, multi_item_attention, rank, segment_rows
 
 __all__ = ["Trie", "attend_row", "beam_attention", "log_softmax_row", "OracleBeam",
-           "exhaustive_scores", "token_id", "key_f32", "ordered_f32"]
+           "exhaustive_scores", "token_id", "key_f32", "ordered_f32", "label_logprobs",
+           "multi_item_attention", "rank", "segment_rows"]

@@ -210,3 +210,86 @@ def test_beam_mutation_is_caught(monkeypatch, golden_dir, name, target, fn):
 def test_beam_class_mutation_is_caught(monkeypatch, golden_dir, cls):
     monkeypatch.setattr(T_beam, "OracleBeam", cls)
     assert _fails(_beam_pins(golden_dir)), cls.__name__
+
+
+# -- multi-item scoring mutations ---------------------------------------------------
+
+import oracle.scoring as osc
+from tests import test_oracle_scoring as T_sc
+
+_orig_mia = osc.multi_item_attention
+_orig_labels = osc.label_logprobs
+_orig_srank = osc.rank
+
+
+def _scoring_pins():
+    return [
+        lambda: T_sc.test_matches_sdpa_on_the_joined_sequence(0, 4, 2, 16, 23, (3, 1, 4, 2)),
+        lambda: T_sc.test_matches_sdpa_on_the_joined_sequence(3, 8, 2, 32, 70, (16, 2, 9)),
+        T_sc.test_other_candidates_and_later_tokens_are_invisible,
+        T_sc.test_equal_keys_give_mean_value,
+        T_sc.test_label_logprobs_match_scipy,
+        T_sc.test_rank_orders_by_score_then_index,
+    ]
+
+
+def _mia_whole_segment(q, pk, pv, sk, sv, seg_lens, rows=None):
+    # every token of a candidate sees the candidate's later tokens too (no causality)
+    hq, d = q.shape[1], q.shape[2]
+    g = hq // pk.shape[0]
+    cand, _ = osc.segment_rows(seg_lens)
+    rows = range(q.shape[0]) if rows is None else rows
+    out = np.zeros((len(rows), hq, d))
+    for i, r in enumerate(rows):
+        own = np.where(cand == cand[r])[0]
+        for h in range(hq):
+            keys = np.concatenate([pk[h // g], sk[own, h // g]])
+            vals = np.concatenate([pv[h // g], sv[own, h // g]])
+            out[i, h], _ = oatt.attend_row(q[r, h], keys, vals, 1 / np.sqrt(d))
+    return out
+
+
+def _mia_sees_previous_candidate(q, pk, pv, sk, sv, seg_lens, rows=None):
+    # the mask leaks the previous candidate's tokens (a plain causal mask over the joined sequence)
+    hq, d = q.shape[1], q.shape[2]
+    g = hq // pk.shape[0]
+    rows = range(q.shape[0]) if rows is None else rows
+    out = np.zeros((len(rows), hq, d))
+    for i, r in enumerate(rows):
+        for h in range(hq):
+            keys = np.concatenate([pk[h // g], sk[:r + 1, h // g]])
+            vals = np.concatenate([pv[h // g], sv[:r + 1, h // g]])
+            out[i, h], _ = oatt.attend_row(q[r, h], keys, vals, 1 / np.sqrt(d))
+    return out
+
+
+def _mia_no_prefix(q, pk, pv, sk, sv, seg_lens, rows=None):
+    return _orig_mia(q, pk[:, :0], pv[:, :0], sk, sv, seg_lens, rows)
+
+
+def _labels_off_by_one(logits, label_ids):
+    V = np.asarray(logits).shape[1]
+    return _orig_labels(logits, [(l + 1) % V for l in label_ids])
+
+
+def _labels_raw_logits(logits, label_ids):
+    return np.asarray(logits, dtype=np.float64)[:, list(label_ids)]
+
+
+def _rank_ties_high_index(scores):
+    s = list(scores)
+    return np.array(sorted(range(len(s)), key=lambda c: (-s[c], -c)), dtype=np.int32)
+
+
+@pytest.mark.parametrize("name,target,fn", [
+    ("segment not causal", "multi_item_attention", _mia_whole_segment),
+    ("previous candidate visible", "multi_item_attention", _mia_sees_previous_candidate),
+    ("prefix dropped", "multi_item_attention", _mia_no_prefix),
+    ("label index off by one", "label_logprobs", _labels_off_by_one),
+    ("labels not normalised", "label_logprobs", _labels_raw_logits),
+    ("ties by higher index", "rank", _rank_ties_high_index),
+])
+def test_scoring_mutation_is_caught(monkeypatch, name, target, fn):
+    monkeypatch.setattr(osc, target, fn)
+    monkeypatch.setattr(T_sc, target, fn)
+    assert _fails(_scoring_pins()), name
