@@ -44,6 +44,8 @@ SYMBOLS = [
     "gr_beam_set_graph_mode", "gr_beam_sync", "gr_beam_results", "gr_beam_path", "gr_beam_status",
     "gr_beam_set_timing", "gr_beam_kernel_stats", "gr_beam_set_wait_limit",
     "gr_constrained_topk_noalloc", "gr_status_str", "gr_last_error",
+    "gr_score_workspace_bytes", "gr_score_create", "gr_score_destroy", "gr_score_rows", "gr_score_attn",
+    "gr_score_labels", "gr_score_status",
 ]
 
 
@@ -61,6 +63,22 @@ class GrRequest(ctypes.Structure):
 class GrBuffers(ctypes.Structure):
     _fields_ = [("ctx_k", ctypes.c_void_p), ("ctx_v", ctypes.c_void_p), ("beam_k", ctypes.c_void_p),
                 ("beam_v", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class GrScoreConfig(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("vocab", ctypes.c_int), ("pool_tokens", ctypes.c_int64),
+                ("n_labels", ctypes.c_int), ("label_ids", ctypes.c_void_p)]
+
+
+class GrScoreRequest(ctypes.Structure):
+    _fields_ = [("ctx_offset", ctypes.c_int64), ("ctx_len", ctypes.c_int), ("n_candidates", ctypes.c_int),
+                ("seg_lens", ctypes.c_void_p)]
+
+
+class GrScoreBuffers(ctypes.Structure):
+    _fields_ = [("ctx_k", ctypes.c_void_p), ("ctx_v", ctypes.c_void_p), ("seg_k", ctypes.c_void_p),
+                ("seg_v", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class GrError(RuntimeError):
@@ -109,6 +127,13 @@ def lib() -> ctypes.CDLL:
             "gr_beam_set_wait_limit": [vp, c_i64],
             "gr_constrained_topk_noalloc": [vp, c_i64, c_int, c_int, c_int, c_int, vp, vp, c_int, vp, vp, vp, vp,
                                             vp],
+            "gr_score_workspace_bytes": [P(GrScoreConfig), P(GrScoreRequest), c_int, P(sz)],
+            "gr_score_create": [P(GrScoreConfig), P(GrScoreRequest), c_int, P(GrScoreBuffers), vp, P(vp)],
+            "gr_score_destroy": [vp],
+            "gr_score_rows": [vp, P(c_int), vp, vp],
+            "gr_score_attn": [vp, c_int, vp, vp, vp],
+            "gr_score_labels": [vp, vp, c_i64, vp, vp, vp],
+            "gr_score_status": [vp, c_int, vp],
             "gr_status_str": [c_int],
             "gr_last_error": [],
         }
@@ -309,3 +334,64 @@ class Beam:
 
     def set_wait_limit(self, ns: int) -> None:
         check(lib().gr_beam_set_wait_limit(self.handle, ns))
+
+
+class Score:
+    """Multi-item candidate scoring of one batch of requests (gr_score handle + its buffers)."""
+
+    def __init__(self, n_layers: int, n_q_heads: int, n_kv_heads: int, head_dim: int, vocab: int,
+                 label_ids: Sequence[int], ctx_k, ctx_v, requests: Sequence[Tuple[int, int, Sequence[int]]],
+                 device="cuda"):
+        """ctx_k / ctx_v: bf16 [n_layers, n_kv_heads, pool_tokens, head_dim];
+        requests: (prefix ctx_offset, prefix ctx_len, tokens of each candidate) per request."""
+        import torch
+        self._labels = np.ascontiguousarray(label_ids, dtype=np.int32)
+        self.cfg = GrScoreConfig(n_layers, n_q_heads, n_kv_heads, head_dim, vocab, ctx_k.shape[2],
+                                 len(self._labels), self._labels.ctypes.data)
+        self._segs = [np.ascontiguousarray(seg, dtype=np.int32) for (_, _, seg) in requests]
+        n = len(requests)
+        self.reqs = (GrScoreRequest * n)(*[GrScoreRequest(o, l, len(sg), sg.ctypes.data)
+                                           for (o, l, _), sg in zip(requests, self._segs)])
+        self.ctx_k, self.ctx_v = ctx_k, ctx_v
+        self.n_requests = n
+        self.n_labels = len(self._labels)
+        ws = ctypes.c_size_t()
+        check(lib().gr_score_workspace_bytes(ctypes.byref(self.cfg), self.reqs, n, ctypes.byref(ws)))
+        self.rows = int(sum(int(sg.sum()) for sg in self._segs))
+        self.n_candidates = int(sum(len(sg) for sg in self._segs))
+        self.workspace = torch.empty(ws.value, dtype=torch.uint8, device=device)
+        shape = (n_layers, self.rows, n_kv_heads, head_dim)
+        self.seg_k = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.seg_v = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        bufs = GrScoreBuffers(ctx_k.data_ptr(), ctx_v.data_ptr(), self.seg_k.data_ptr(), self.seg_v.data_ptr(),
+                              self.workspace.data_ptr(), self.workspace.numel())
+        h = ctypes.c_void_p()
+        check(lib().gr_score_create(ctypes.byref(self.cfg), self.reqs, n, ctypes.byref(bufs), _stream_ptr(),
+                                    ctypes.byref(h)))
+        self.handle = h
+        rows = ctypes.c_int()
+        ro, co = (ctypes.c_int * (n + 1))(), (ctypes.c_int * (n + 1))()
+        check(lib().gr_score_rows(self.handle, ctypes.byref(rows), ro, co))
+        assert rows.value == self.rows
+        self.row_offsets, self.cand_offsets = list(ro), list(co)
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.gr_score_destroy(self.handle)
+            self.handle = None
+
+    def attn(self, layer: int, q, out, stream=None) -> None:
+        check(lib().gr_score_attn(self.handle, layer, q.data_ptr(), out.data_ptr(), _stream_ptr(stream)))
+
+    def labels(self, logits, ld: Optional[int] = None, ranking: bool = True, stream=None):
+        """(log-probs float32 [n_candidates, n_labels], ranking int32 [n_candidates] or None)."""
+        import torch
+        ld = logits.stride(0) if ld is None else ld
+        lp = torch.empty((self.n_candidates, self.n_labels), dtype=torch.float32, device=logits.device)
+        rk = torch.empty(self.n_candidates, dtype=torch.int32, device=logits.device) if ranking else None
+        check(lib().gr_score_labels(self.handle, logits.data_ptr(), ld, lp.data_ptr(), _ptr(rk),
+                                    _stream_ptr(stream)))
+        return lp, rk
+
+    def status(self, clear: bool = False, stream=None) -> int:
+        return lib().gr_score_status(self.handle, 1 if clear else 0, _stream_ptr(stream))

@@ -1012,6 +1012,312 @@ extern "C" gr_status gr_beam_set_wait_limit(gr_beam* h, int64_t nanoseconds) {
     return GR_OK;
 }
 
+// ---------------------------------------------------------------------------
+// multi-item candidate scoring
+// ---------------------------------------------------------------------------
+namespace {
+struct ScoreLayout {
+    size_t req, tmaps, jobs, cta_jobs, units, seg_first, seg_pos, cand_off, labels, tables_end, status, o_part,
+        lse_part, piece_flag, total;
+};
+
+gr_status check_score(const gr_score_config* c, const gr_score_request* reqs, int n) {
+    if (c == nullptr || (reqs == nullptr && n > 0)) return fail(GR_ERR_INVALID_ARG, "NULL config or requests");
+    if (n < 1) return fail(GR_ERR_INVALID_ARG, "n_requests must be >= 1");
+    if (c->n_layers < 1) return fail(GR_ERR_INVALID_ARG, "n_layers must be >= 1");
+    if (c->n_kv_heads < 1 || c->n_q_heads < c->n_kv_heads || c->n_q_heads % c->n_kv_heads != 0)
+        return fail(GR_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+    const int G = c->n_q_heads / c->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+        return fail(GR_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4, 8 or 16 (got %d)", G);
+    if (c->head_dim != 64 && c->head_dim != 128) return fail(GR_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (c->vocab < 1 || c->pool_tokens < 1) return fail(GR_ERR_INVALID_ARG, "vocab and pool_tokens must be >= 1");
+    if (c->n_labels < 1 || c->n_labels > 16 || c->label_ids == nullptr)
+        return fail(GR_ERR_INVALID_ARG, "n_labels must be 1..16 with label_ids given");
+    for (int k = 0; k < c->n_labels; ++k)
+        if (c->label_ids[k] < 0 || c->label_ids[k] >= c->vocab)
+            return fail(GR_ERR_INVALID_ARG, "label %d: token %d outside the vocabulary", k, c->label_ids[k]);
+    for (int r = 0; r < n; ++r) {
+        const gr_score_request& q = reqs[r];
+        if (q.ctx_len < 1 || q.ctx_offset < 0 || q.ctx_offset + q.ctx_len > c->pool_tokens)
+            return fail(GR_ERR_INVALID_ARG, "request %d: prefix outside the pool", r);
+        if (q.n_candidates < 1 || q.n_candidates > kMaxCandidates)
+            return fail(GR_ERR_CAPACITY, "request %d: n_candidates must be in 1..%d", r, kMaxCandidates);
+        if (q.seg_lens == nullptr) return fail(GR_ERR_INVALID_ARG, "request %d: seg_lens is NULL", r);
+        for (int k = 0; k < q.n_candidates; ++k)
+            if (q.seg_lens[k] < 1 || q.seg_lens[k] > kMaxSegment)
+                return fail(GR_ERR_CAPACITY, "request %d, candidate %d: %d tokens (1..%d)", r, k, q.seg_lens[k],
+                            kMaxSegment);
+    }
+    return GR_OK;
+}
+
+// the decode schedule's view of a scoring batch: one "beam" per candidate token
+void score_as_decode(const gr_score_config* c, const gr_score_request* reqs, int n, gr_config* dc,
+                     std::vector<gr_request>& dr, int* rows) {
+    *dc = gr_config{};
+    dc->n_layers = c->n_layers;
+    dc->n_q_heads = c->n_q_heads;
+    dc->n_kv_heads = c->n_kv_heads;
+    dc->head_dim = c->head_dim;
+    dc->vocab = c->vocab;
+    dc->n_levels = 1;
+    dc->codes_per_level = 1;
+    dc->pool_tokens = c->pool_tokens;
+    dr.assign(n, gr_request{});
+    *rows = 0;
+    for (int r = 0; r < n; ++r) {
+        int w = 0;
+        for (int k = 0; k < reqs[r].n_candidates; ++k) w += reqs[r].seg_lens[k];
+        dr[r].ctx_offset = reqs[r].ctx_offset;
+        dr[r].ctx_len = reqs[r].ctx_len;
+        dr[r].beam_width = w;
+        *rows += w;
+    }
+}
+
+ScoreLayout score_layout(int n, int rows, int n_cand, int n_labels, int head_dim, const Caps& k) {
+    ScoreLayout w{};
+    size_t o = 0;
+    auto take = [&](size_t bytes, size_t align = 256) {
+        o = align_up(o, align);
+        size_t r = o;
+        o += bytes;
+        return r;
+    };
+    w.req = take(sizeof(GrReqDev) * n);
+    w.tmaps = take(sizeof(CUtensorMap) * 2 * n, 128);
+    w.jobs = take(sizeof(GrAttnJob) * k.jobs);
+    w.cta_jobs = take(sizeof(int2) * k.ctas);
+    w.units = take(sizeof(GrAttnUnit) * k.units);
+    w.seg_first = take(4ull * rows);
+    w.seg_pos = take(4ull * rows);
+    w.cand_off = take(4ull * (n + 1));
+    w.labels = take(4ull * n_labels);
+    w.tables_end = align_up(o, 256);
+    w.status = take(16);
+    w.o_part = take(4ull * k.jobs * kUnitRows * head_dim);
+    w.lse_part = take(4ull * k.jobs * kUnitRows);
+    w.piece_flag = take(4ull * k.jobs * kUnitRows);
+    w.total = align_up(o, 256);
+    return w;
+}
+}  // namespace
+
+struct gr_score {
+    gr_score_config cfg{};
+    std::vector<int32_t> labels;
+    int n_req = 0, rows = 0, n_cand = 0;
+    std::vector<int> row_off, cand_off;
+    GrState st{};
+    Caps caps{};
+    ScoreLayout w{};
+    int64_t wait_limit_ns = 2000000000ll;
+};
+
+extern "C" gr_status gr_score_workspace_bytes(const gr_score_config* cfg, const gr_score_request* reqs, int n,
+                                              size_t* bytes) {
+    if (bytes == nullptr) return fail(GR_ERR_INVALID_ARG, "bytes is NULL");
+    gr_status s = check_score(cfg, reqs, n);
+    if (s != GR_OK) return s;
+    int n_sm = device_sm_count();
+    if (n_sm <= 0) n_sm = 148;
+    gr_config dc;
+    std::vector<gr_request> dr;
+    int rows = 0, n_cand = 0;
+    score_as_decode(cfg, reqs, n, &dc, dr, &rows);
+    for (int r = 0; r < n; ++r) n_cand += reqs[r].n_candidates;
+    std::vector<int> uo, nu;
+    Schedule sc = build_schedule(&dc, dr.data(), n, n_sm, uo, nu);
+    *bytes = score_layout(n, rows, n_cand, cfg->n_labels, cfg->head_dim, caps_of(sc, n_sm)).total;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_score_create(const gr_score_config* cfg, const gr_score_request* reqs, int n,
+                                     const gr_score_buffers* bufs, gr_stream_t stream, gr_score** out) {
+    if (out == nullptr || bufs == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL out or buffers");
+    *out = nullptr;
+    gr_status s = check_score(cfg, reqs, n);
+    if (s != GR_OK) return s;
+    if (!bufs->ctx_k || !bufs->ctx_v || !bufs->seg_k || !bufs->seg_v || !bufs->workspace)
+        return fail(GR_ERR_INVALID_ARG, "ctx_k, ctx_v, seg_k, seg_v and workspace must be device pointers");
+    if ((reinterpret_cast<uintptr_t>(bufs->workspace) & 255) != 0)
+        return fail(GR_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(bufs->ctx_k) & 15) != 0 || (reinterpret_cast<uintptr_t>(bufs->ctx_v) & 15) != 0)
+        return fail(GR_ERR_INVALID_ARG, "ctx_k / ctx_v must be 16-byte aligned");
+    const int n_sm = device_sm_count();
+    if (n_sm <= 0) return fail(GR_ERR_CUDA, "no CUDA device");
+    cudaStream_t cs = (cudaStream_t)stream;
+    gr_score* h = nullptr;
+    try {
+        h = new gr_score;
+        h->cfg = *cfg;
+        h->labels.assign(cfg->label_ids, cfg->label_ids + cfg->n_labels);
+        h->cfg.label_ids = h->labels.data();
+        h->n_req = n;
+        gr_config dc;
+        std::vector<gr_request> dr;
+        score_as_decode(cfg, reqs, n, &dc, dr, &h->rows);
+        h->row_off.assign(n + 1, 0);
+        h->cand_off.assign(n + 1, 0);
+        for (int r = 0; r < n; ++r) {
+            h->row_off[r + 1] = h->row_off[r] + dr[r].beam_width;
+            h->cand_off[r + 1] = h->cand_off[r] + reqs[r].n_candidates;
+        }
+        h->n_cand = h->cand_off[n];
+        std::vector<int> unit_off, n_ub;
+        Schedule sc = build_schedule(&dc, dr.data(), n, n_sm, unit_off, n_ub);
+        h->caps = caps_of(sc, n_sm);
+        h->w = score_layout(n, h->rows, h->n_cand, cfg->n_labels, cfg->head_dim, h->caps);
+        const ScoreLayout& w = h->w;
+        if (bufs->workspace_bytes < w.total) {
+            gr_status e = fail(GR_ERR_CAPACITY, "workspace needs %zu bytes, got %zu", w.total, bufs->workspace_bytes);
+            delete h;
+            return e;
+        }
+        uint8_t* ws = static_cast<uint8_t*>(bufs->workspace);
+        GrState& st = h->st;
+        st.req = reinterpret_cast<GrReqDev*>(ws + w.req);
+        st.n_req = n;
+        st.rows = h->rows;
+        st.n_levels = 1;
+        st.vocab = cfg->vocab;
+        st.n_layers = cfg->n_layers;
+        st.n_q_heads = cfg->n_q_heads;
+        st.n_kv_heads = cfg->n_kv_heads;
+        st.head_dim = cfg->head_dim;
+        st.pool_tokens = cfg->pool_tokens;
+        st.status = reinterpret_cast<int32_t*>(ws + w.status);
+        st.tmaps = reinterpret_cast<CUtensorMap*>(ws + w.tmaps);
+        st.jobs = reinterpret_cast<GrAttnJob*>(ws + w.jobs);
+        st.cta_jobs = reinterpret_cast<int2*>(ws + w.cta_jobs);
+        st.units = reinterpret_cast<GrAttnUnit*>(ws + w.units);
+        st.o_part = reinterpret_cast<float*>(ws + w.o_part);
+        st.lse_part = reinterpret_cast<float*>(ws + w.lse_part);
+        st.piece_flag = reinterpret_cast<uint32_t*>(ws + w.piece_flag);
+        st.beam_k = static_cast<const uint16_t*>(bufs->seg_k);
+        st.beam_v = static_cast<const uint16_t*>(bufs->seg_v);
+        st.seg_first = reinterpret_cast<const int32_t*>(ws + w.seg_first);
+        st.seg_pos = reinterpret_cast<const int32_t*>(ws + w.seg_pos);
+        st.n_units = (int)sc.units.size();
+        st.n_jobs = (int)sc.jobs.size();
+        st.n_cta = (int)sc.cta_jobs.size();
+        // host image of the tables
+        std::vector<uint8_t> img(w.tables_end, 0);
+        GrReqDev* rq = reinterpret_cast<GrReqDev*>(img.data() + w.req);
+        CUtensorMap* tm = reinterpret_cast<CUtensorMap*>(img.data() + w.tmaps);
+        int32_t* sf = reinterpret_cast<int32_t*>(img.data() + w.seg_first);
+        int32_t* sp = reinterpret_cast<int32_t*>(img.data() + w.seg_pos);
+        const int D = cfg->head_dim;
+        const uint64_t zdim = (uint64_t)cfg->n_layers * cfg->n_kv_heads;
+        for (int r = 0; r < n; ++r) {
+            GrReqDev d{};
+            d.row_off = h->row_off[r];
+            d.width = dr[r].beam_width;
+            d.ctx_len = reqs[r].ctx_len;
+            d.n_levels = 1;
+            d.unit_off = unit_off[r];
+            d.n_ub = n_ub[r];
+            d.ctx_off = reqs[r].ctx_offset;
+            rq[r] = d;
+            int row = h->row_off[r];
+            for (int k = 0; k < reqs[r].n_candidates; ++k)
+                for (int p = 0; p < reqs[r].seg_lens[k]; ++p, ++row) {
+                    sf[row] = row - p;
+                    sp[row] = p;
+                }
+            const uint64_t off = (uint64_t)reqs[r].ctx_offset * D * 2;
+            const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)cfg->pool_tokens * D * 2;
+            if ((s = make_tmap_3d(&tm[2 * r], static_cast<const uint8_t*>(bufs->ctx_k) + off, D, reqs[r].ctx_len, zdim,
+                                  s1, s2, 64, kTileKeys, 1)) != GR_OK ||
+                (s = make_tmap_3d(&tm[2 * r + 1], static_cast<const uint8_t*>(bufs->ctx_v) + off, D, reqs[r].ctx_len,
+                                  zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK) {
+                delete h;
+                return s;
+            }
+        }
+        memcpy(img.data() + w.jobs, sc.jobs.data(), sizeof(GrAttnJob) * sc.jobs.size());
+        memcpy(img.data() + w.cta_jobs, sc.cta_jobs.data(), sizeof(int2) * sc.cta_jobs.size());
+        memcpy(img.data() + w.units, sc.units.data(), sizeof(GrAttnUnit) * sc.units.size());
+        memcpy(img.data() + w.cand_off, h->cand_off.data(), 4ull * (n + 1));
+        memcpy(img.data() + w.labels, h->labels.data(), 4ull * h->labels.size());
+        cudaError_t e = cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaMemsetAsync(ws + w.status, 0, 16, cs);
+        if (e == cudaSuccess) e = cudaMemsetAsync(st.piece_flag, 0, 4ull * h->caps.jobs * kUnitRows, cs);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);  // img is released on return
+        if (e != cudaSuccess) {
+            delete h;
+            return cuda_fail(e, "workspace upload");
+        }
+    } catch (const std::bad_alloc&) {
+        delete h;
+        return fail(GR_ERR_CAPACITY, "host allocation failed");
+    }
+    *out = h;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_score_destroy(gr_score* h) {
+    delete h;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_score_rows(const gr_score* h, int* rows_total, int* row_offsets, int* cand_offsets) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    if (rows_total) *rows_total = h->rows;
+    for (int r = 0; r <= h->n_req; ++r) {
+        if (row_offsets) row_offsets[r] = h->row_off[r];
+        if (cand_offsets) cand_offsets[r] = h->cand_off[r];
+    }
+    return GR_OK;
+}
+
+extern "C" gr_status gr_score_attn(gr_score* h, int layer, const void* q, void* out, gr_stream_t stream) {
+    if (h == nullptr || q == nullptr || out == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (layer < 0 || layer >= h->cfg.n_layers) return fail(GR_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if ((reinterpret_cast<uintptr_t>(q) & 15) != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0)
+        return fail(GR_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+    const gr_score_config& c = h->cfg;
+    const int G = c.n_q_heads / c.n_kv_heads;
+    CUtensorMap qmap;
+    gr_status s = make_tmap_3d(&qmap, q, c.head_dim, c.n_q_heads, h->rows, (uint64_t)c.head_dim * 2,
+                               (uint64_t)c.n_q_heads * c.head_dim * 2, 64, G, kTileRows / G);
+    if (s != GR_OK) return s;
+    cudaError_t e = launch_score_attn(h->st, qmap, layer, static_cast<const uint16_t*>(q), static_cast<uint16_t*>(out),
+                                      h->wait_limit_ns, (cudaStream_t)stream);
+    return e == cudaSuccess ? GR_OK : cuda_fail(e, "kernel launch");
+}
+
+extern "C" gr_status gr_score_labels(gr_score* h, const float* logits, int64_t ld, float* logprobs, int32_t* ranking,
+                                     gr_stream_t stream) {
+    if (h == nullptr || logits == nullptr || logprobs == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (ld < h->cfg.vocab || ld % 4 != 0) return fail(GR_ERR_INVALID_ARG, "ld must be >= vocab and a multiple of 4");
+    if ((reinterpret_cast<uintptr_t>(logits) & 15) != 0) return fail(GR_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+    cudaStream_t cs = (cudaStream_t)stream;
+    const uint8_t* ws = reinterpret_cast<const uint8_t*>(h->st.req);
+    const int32_t* labels = reinterpret_cast<const int32_t*>(ws + h->w.labels);
+    cudaError_t e = launch_label_logprobs(logits, ld, h->cfg.vocab, labels, h->cfg.n_labels, h->n_cand, logprobs,
+                                          h->st.status, cs);
+    if (e == cudaSuccess && ranking != nullptr)
+        e = launch_rank(logprobs, h->cfg.n_labels, reinterpret_cast<const int32_t*>(ws + h->w.cand_off), h->n_req,
+                        ranking, h->st.status, cs);
+    return e == cudaSuccess ? GR_OK : cuda_fail(e, "kernel launch");
+}
+
+extern "C" gr_status gr_score_status(gr_score* h, int clear_flag, gr_stream_t stream) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    cudaStream_t cs = (cudaStream_t)stream;
+    int w = 0;
+    GR_CUDA(cudaMemcpyAsync(&w, h->st.status, 4, cudaMemcpyDeviceToHost, cs), "status read");
+    GR_CUDA(cudaStreamSynchronize(cs), "status sync");
+    if (clear_flag && w != 0) {
+        GR_CUDA(cudaMemsetAsync(h->st.status, 0, 16, cs), "status clear");
+        GR_CUDA(cudaMemsetAsync(h->st.piece_flag, 0, 4ull * h->caps.jobs * kUnitRows, cs), "flag clear");
+        GR_CUDA(cudaStreamSynchronize(cs), "status clear sync");
+    }
+    return status_from_word(w);
+}
+
 extern "C" const char* gr_status_str(gr_status s) {
     switch (s) {
         case GR_OK: return "GR_OK";

@@ -15,6 +15,8 @@ namespace grb {
 constexpr int kMaxBeam = 1024;        // W_r upper bound (one CTA of the selection kernel)
 constexpr int kMaxCodes = 1024;       // C upper bound
 constexpr int kMaxLevels = 8;         // L upper bound
+constexpr int kMaxSegment = 16;       // tokens of one scored candidate (multi-item scoring)
+constexpr int kMaxPriv = 16;          // private keys of one query row (BeamKV path or own segment)
 constexpr int kTileRows = 128;        // query rows per tensor-core tile (TMEM lanes)
 constexpr int kTileKeys = 128;        // context keys per tile
 constexpr int kUnitRows = 256;        // query rows per attention unit (two tiles)
@@ -98,8 +100,11 @@ struct GrState {
     float* o_part;      // [n_jobs][D][kUnitRows] pieces of split units (later key ranges), column-major
     float* lse_part;    // [n_jobs][kUnitRows]
     uint32_t* piece_flag; // [n_jobs][kUnitRows] 1 = piece row published and not yet merged
-    const uint16_t* beam_k; // bf16 [NL][L-1][rows][Hkv][D]
+    const uint16_t* beam_k; // bf16 [NL][L-1][rows][Hkv][D]; scoring: the candidates' own tokens [NL][rows][Hkv][D]
     const uint16_t* beam_v;
+    // multi-item scoring: row -> first row of its candidate, and its position in the candidate
+    const int32_t* seg_first;
+    const int32_t* seg_pos;
 
     // results staging
     int32_t* res_codes; // [rows][L]
@@ -117,10 +122,17 @@ cudaError_t launch_logsoftmax_gather(const GrState& st, const float* logits, int
 cudaError_t launch_topk_select(const GrState& st, cudaStream_t s);
 cudaError_t launch_advance(const GrState& st, cudaStream_t s);
 cudaError_t launch_results(const GrState& st, cudaStream_t s);
+constexpr int kMaxCandidates = 1024;  // candidates of one scored request (one CTA ranks them)
+cudaError_t launch_label_logprobs(const float* logits, int64_t ld, int vocab, const int32_t* labels, int n_labels,
+                                  int n_rows, float* out, int32_t* status, cudaStream_t s);
+cudaError_t launch_rank(const float* lp, int n_labels, const int32_t* cand_off, int n_req, int32_t* rank_out,
+                        int32_t* status, cudaStream_t s);
 
 // ---- launchers (k_attn.cu) ----
 cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes);
 cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
                             uint16_t* out, int64_t wait_limit_ns, cudaStream_t s);
+cudaError_t launch_score_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
+                              uint16_t* out, int64_t wait_limit_ns, cudaStream_t s);
 
 }  // namespace grb

@@ -313,7 +313,9 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t value, 
 // a unit takes part in a launch when its request is at a decode step 1 <= t_r < L_r
 // (level 0 has no BeamKV and needs no attention; t_r == L_r is finished).  Every role of
 // the CTA reads the same device-resident step, so they skip the same jobs.
+template <bool kScore>
 __device__ __forceinline__ bool decoding(const GrState& st, const GrAttnUnit& U) {
+    if constexpr (kScore) return true;  // multi-item scoring: one pass, every unit takes part
     const int t = st.req_step[U.req];
     return t >= 1 && t < st.req[U.req].n_levels;
 }
@@ -347,7 +349,7 @@ enum Bar {
 
 constexpr int kAttnThreads = 384;
 
-template <int D>
+template <int D, bool kScore>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, const uint16_t* __restrict__ q,
            uint16_t* __restrict__ out, float scale_log2, float scale, int64_t wait_limit_ns) {
@@ -405,7 +407,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 const GrAttnJob J = st.jobs[jb];
                 const GrAttnUnit U = st.units[J.unit];
                 const GrReqDev& R = st.req[U.req];
-                if (!decoding(st, U)) continue;
+                if (!decoding<kScore>(st, U)) continue;
                 const CUtensorMap* km = st.tmaps + 2 * U.req;
                 const CUtensorMap* vm = km + 1;
                 if (jb == jr.x || st.jobs[jb - 1].unit != J.unit) {
@@ -469,7 +471,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             for (int jb = jr.x; jb < jr.y && ok; ++jb) {
                 const GrAttnJob J = st.jobs[jb];
                 const GrAttnUnit U = st.units[J.unit];
-                if (!decoding(st, U)) continue;
+                if (!decoding<kScore>(st, U)) continue;
                 const int nqt = U.nqt;
                 const int n = J.t1 - J.t0;
                 if (!(ok = wait1(bar(B_Q_FULL), qcnt & 1, wt))) break;
@@ -559,8 +561,8 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
         for (int jb = jr.x; jb < jr.y && ok; ++jb) {
             const GrAttnJob J = st.jobs[jb];
             const GrAttnUnit U = st.units[J.unit];
-            if (i >= U.nqt || !decoding(st, U)) continue;
-            const int t = st.req_step[U.req];  // 1 <= t < L_r: BeamKV levels 0..t-1 exist
+            if (i >= U.nqt || !decoding<kScore>(st, U)) continue;
+            const int t = kScore ? 0 : st.req_step[U.req];  // decode: 1 <= t < L_r, BeamKV levels 0..t-1
             const int ctx_len = st.req[U.req].ctx_len;
             const int n = J.t1 - J.t0;
             const bool merger = (J.slot == U.first_slot);
@@ -569,13 +571,32 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             const int b = U.beam0 + i * (kTileRows / G) + row_t / G;
             const int g = row_t % G;
             const bool row_ok = b < R.width;
-            const bool live = row_ok && b < st.n_beams[U.req * (st.n_levels + 1) + t];
+            const bool live = row_ok && (kScore || b < st.n_beams[U.req * (st.n_levels + 1) + t]);
             const int64_t orow_idx = (int64_t)(R.row_off + b) * st.n_q_heads + U.head * G + g;
             const int L = st.n_levels;
-            const int32_t* path = st.path + ((int64_t)(t - 1) * st.rows + R.row_off + b) * L;
-            if (merger && live) prefetch_l2(path);
+            // The row's private keys.  Decode: the t BeamKV tokens on the beam's path, one per
+            // level, found through its ancestry row.  Scoring: the tokens of the row's own
+            // candidate up to itself.  The warp's loops run to t_w (the largest count of its
+            // rows); a row's surplus keys read row 0 of the pool and get weight 0.
+            const int32_t* path = kScore ? nullptr : st.path + ((int64_t)(t - 1) * st.rows + R.row_off + b) * L;
+            int n_priv = 0, seg0 = 0;
+            if constexpr (kScore) {
+                if (live) {
+                    n_priv = st.seg_pos[R.row_off + b] + 1;
+                    seg0 = st.seg_first[R.row_off + b];
+                }
+            } else {
+                n_priv = live ? t : 0;
+                if (merger && live) prefetch_l2(path);
+            }
+            const int t_w = kScore ? __reduce_max_sync(0xffffffffu, n_priv) : t;
+            auto priv_row = [&](int j) -> int64_t {
+                if (j >= n_priv) return 0;
+                if constexpr (kScore) return ((int64_t)layer * st.rows + seg0 + j) * st.n_kv_heads + U.head;
+                return (((int64_t)layer * (L - 1) + j) * st.rows + R.row_off + path[j]) * st.n_kv_heads + U.head;
+            };
             const int jj_pf = n > 2 ? n - 2 : 0;  // tile at which the merge inputs are prefetched
-            int64_t kvj[kMaxLevels];
+            int64_t kvj[kMaxPriv];
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int jj = 0; jj < n; ++jj) {
                 if (!(ok = wait_warp(bar(B_S_FULL + i), tiles & 1, wt))) break;
@@ -650,10 +671,8 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                     if (live) {
                         const char* qrow = reinterpret_cast<const char*>(q + orow_idx * D);
                         for (int o = 0; o < D * 2; o += 128) prefetch_l2(qrow + o);
-                        for (int j = 0; j < t; ++j) {
-                            const int slot = path[j];
-                            kvj[j] = (((int64_t)layer * (L - 1) + j) * st.rows + R.row_off + slot) * st.n_kv_heads +
-                                     U.head;
+                        for (int j = 0; j < n_priv; ++j) {
+                            kvj[j] = priv_row(j);
                             const char* kr = reinterpret_cast<const char*>(st.beam_k + kvj[j] * D);
                             const char* vr = reinterpret_cast<const char*>(st.beam_v + kvj[j] * D);
                             for (int o = 0; o < D * 2; o += 128) { prefetch_l2(kr + o); prefetch_l2(vr + o); }
@@ -712,8 +731,9 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             if (__any_sync(0xffffffffu, !have)) { ok = false; break; }
             __threadfence();
             // ---- beam scores q . k_j / sqrt(D)
-            float sj[kMaxLevels];
-            for (int j = 0; j < t; ++j) {
+            float sj[kMaxPriv];
+            for (int j = 0; j < t_w; ++j) {
+                kvj[j] = priv_row(j);
                 const uint16_t* qp_mine = q + (live ? orow_idx : 0) * D;
                 const uint16_t* kp_mine = st.beam_k + (live ? kvj[j] : 0) * D;
                 float mine = 0.f;
@@ -768,21 +788,21 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                     }
                     mine = d0 + d1;
                 }
-                sj[j] = mine * scale;
+                sj[j] = j < n_priv ? mine * scale : -CUDART_INF_F;
             }
             // ---- weights of the parts (own piece, published pieces, beam tokens)
             const float* lse_col = st.lse_part + (int64_t)U.first_slot * kUnitRows + prow;
             float M = lse_own;
             for (int pp = 1; pp <= n_other; ++pp) M = fmaxf(M, __ldcg(lse_col + (int64_t)pp * kUnitRows));
-            for (int j = 0; j < t; ++j) M = fmaxf(M, sj[j]);
+            for (int j = 0; j < t_w; ++j) M = fmaxf(M, sj[j]);
             float den = __expf(lse_own - M);
             for (int pp = 1; pp <= n_other; ++pp) den += __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
-            float w_j[kMaxLevels];
-            for (int j = 0; j < t; ++j) { w_j[j] = __expf(sj[j] - M); den += w_j[j]; }
+            float w_j[kMaxPriv];
+            for (int j = 0; j < t_w; ++j) { w_j[j] = __expf(sj[j] - M); den += w_j[j]; }
             // dead beams come out as exact zeros: none of their (unwritten) inputs is used
             const float inv_den = 1.f / den;
             const float c_own = live ? __expf(lse_own - M) * inv_l * inv_den : 0.f;
-            for (int j = 0; j < t; ++j) w_j[j] = live ? w_j[j] * inv_den : 0.f;
+            for (int j = 0; j < t_w; ++j) w_j[j] = live ? w_j[j] * inv_den : 0.f;
             float* a = reinterpret_cast<float*>(ov);  // the row accumulates in place of O
 #pragma unroll
             for (int c = 0; c < D; ++c) a[c] = live ? __uint_as_float(ov[c]) * c_own : 0.f;
@@ -800,8 +820,8 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 }
                 st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
             }
-            // ---- BeamKV values
-            for (int j = 0; j < t; ++j) {
+            // ---- BeamKV values (scoring: the candidate's own values)
+            for (int j = 0; j < t_w; ++j) {
                 if (staged) {
                     const uint16_t* vp_mine = st.beam_v + (live ? kvj[j] : 0) * D;
                     __syncwarp();
@@ -882,12 +902,12 @@ cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes) {
     return cudaSuccess;
 }
 
-template <int D>
+template <int D, bool kScore>
 cudaError_t launch_ctx_attn_d(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
                               uint16_t* out, float scale_log2, float scale, int64_t wait_limit_ns, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_ctx_attn<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(k_ctx_attn<D, kScore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Plan<D>::kBytes);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -904,16 +924,30 @@ cudaError_t launch_ctx_attn_d(const GrState& st, const CUtensorMap& qmap, int la
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_ctx_attn<D>, qmap, st, layer, q, out, scale_log2, scale, wait_limit_ns);
+    return cudaLaunchKernelEx(&cfg, k_ctx_attn<D, kScore>, qmap, st, layer, q, out, scale_log2, scale,
+                              wait_limit_ns);
+}
+
+template <bool kScore>
+cudaError_t launch_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q, uint16_t* out,
+                        int64_t wait_limit_ns, cudaStream_t s) {
+    const float scale = 1.f / sqrtf((float)st.head_dim);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    if (st.head_dim == 128)
+        return launch_ctx_attn_d<128, kScore>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
+    if (st.head_dim == 64)
+        return launch_ctx_attn_d<64, kScore>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
                             uint16_t* out, int64_t wait_limit_ns, cudaStream_t s) {
-    const float scale = 1.f / sqrtf((float)st.head_dim);
-    const float scale_log2 = scale * 1.4426950408889634f;
-    if (st.head_dim == 128) return launch_ctx_attn_d<128>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
-    if (st.head_dim == 64) return launch_ctx_attn_d<64>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
-    return cudaErrorInvalidValue;
+    return launch_attn<false>(st, qmap, layer, q, out, wait_limit_ns, s);
+}
+
+cudaError_t launch_score_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
+                              uint16_t* out, int64_t wait_limit_ns, cudaStream_t s) {
+    return launch_attn<true>(st, qmap, layer, q, out, wait_limit_ns, s);
 }
 
 }  // namespace grb

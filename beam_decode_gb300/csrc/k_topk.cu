@@ -71,6 +71,74 @@ __device__ __forceinline__ bool row_live(const GrState& st, int row, int& r, int
 // ---------------------------------------------------------------------------
 constexpr int kLsThreads = 256;
 
+// Natural-log log-sum-exp of one logit row of V floats (16-byte aligned), split over the
+// kLogitCluster CTAs of a cluster: each CTA reduces a quarter of the row with 16-byte
+// loads into a running (max, sum), the cluster combines the four partials through
+// distributed shared memory in a fixed order, and every CTA returns the same value.
+__device__ __forceinline__ float cluster_row_lse(const float* __restrict__ x, int V, cg::cluster_group& cluster,
+                                                 int part, float* red_m, float* red_s, float* part_ms) {
+    const int n4 = V >> 2;
+    const int b0 = (int)((int64_t)n4 * part / kLogitCluster);
+    const int b1 = (int)((int64_t)n4 * (part + 1) / kLogitCluster);
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    float m = -CUDART_INF_F, s = 0.f;
+    int i = b0 + threadIdx.x;
+    // 4 independent 16-byte loads in flight per thread
+    for (; i + 3 * kLsThreads < b1; i += 4 * kLsThreads) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldcs(x4 + i + u * kLsThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float cm = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
+            if (cm > m) { s *= exp2f((m - cm) * CUDART_L2E_F); m = cm; }
+            const float ml = m * CUDART_L2E_F;
+            s += exp2f(fmaf(v[u].x, CUDART_L2E_F, -ml)) + exp2f(fmaf(v[u].y, CUDART_L2E_F, -ml)) +
+                 exp2f(fmaf(v[u].z, CUDART_L2E_F, -ml)) + exp2f(fmaf(v[u].w, CUDART_L2E_F, -ml));
+        }
+    }
+    for (; i < b1; i += kLsThreads) {
+        float4 v = __ldcs(x4 + i);
+        float cm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+        if (cm > m) { s *= exp2f((m - cm) * CUDART_L2E_F); m = cm; }
+        const float ml = m * CUDART_L2E_F;
+        s += exp2f(fmaf(v.x, CUDART_L2E_F, -ml)) + exp2f(fmaf(v.y, CUDART_L2E_F, -ml)) +
+             exp2f(fmaf(v.z, CUDART_L2E_F, -ml)) + exp2f(fmaf(v.w, CUDART_L2E_F, -ml));
+    }
+    if (part == kLogitCluster - 1) {  // ragged tail of a row whose length is not a multiple of 4
+        for (int j = (n4 << 2) + threadIdx.x; j < V; j += kLsThreads) {
+            float v = x[j];
+            lse_merge(m, s, v, 1.f);
+        }
+    }
+    // warp, then block
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+        lse_merge(m, s, m2, s2);
+    }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) { red_m[w] = m; red_s[w] = s; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float mm = red_m[0], ss = red_s[0];
+        for (int k = 1; k < kLsThreads / 32; ++k) lse_merge(mm, ss, red_m[k], red_s[k]);
+        part_ms[0] = mm;
+        part_ms[1] = ss;
+    }
+    cluster.sync();
+    // every CTA combines the four partials in the same order
+    float mm = -CUDART_INF_F, ss = 0.f;
+    for (int k = 0; k < kLogitCluster; ++k) {
+        const float* pk = cluster.map_shared_rank(part_ms, k);
+        lse_merge(mm, ss, pk[0], pk[1]);
+    }
+    cluster.sync();  // keep every CTA's shared memory alive until all have read it
+    return mm + logf(ss);
+}
+
+
 __global__ void __cluster_dims__(kLogitCluster, 1, 1) __launch_bounds__(kLsThreads)
 k_logsoftmax_gather(GrState st, const float* __restrict__ logits, int64_t ld,
                     float* __restrict__ logprobs_out, float* __restrict__ lse_out,
@@ -89,65 +157,7 @@ k_logsoftmax_gather(GrState st, const float* __restrict__ logits, int64_t ld,
     const int V = st.vocab;
     float lse;
     if (lse_in == nullptr) {
-        const int n4 = V >> 2;
-        const int b0 = (int)((int64_t)n4 * part / kLogitCluster);
-        const int b1 = (int)((int64_t)n4 * (part + 1) / kLogitCluster);
-        const float4* x4 = reinterpret_cast<const float4*>(x);
-        float m = -CUDART_INF_F, s = 0.f;
-        int i = b0 + threadIdx.x;
-        // 4 independent 16-byte loads in flight per thread
-        for (; i + 3 * kLsThreads < b1; i += 4 * kLsThreads) {
-            float4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = __ldcs(x4 + i + u * kLsThreads);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float cm = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
-                if (cm > m) { s *= exp2f((m - cm) * CUDART_L2E_F); m = cm; }
-                const float ml = m * CUDART_L2E_F;
-                s += exp2f(fmaf(v[u].x, CUDART_L2E_F, -ml)) + exp2f(fmaf(v[u].y, CUDART_L2E_F, -ml)) +
-                     exp2f(fmaf(v[u].z, CUDART_L2E_F, -ml)) + exp2f(fmaf(v[u].w, CUDART_L2E_F, -ml));
-            }
-        }
-        for (; i < b1; i += kLsThreads) {
-            float4 v = __ldcs(x4 + i);
-            float cm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-            if (cm > m) { s *= exp2f((m - cm) * CUDART_L2E_F); m = cm; }
-            const float ml = m * CUDART_L2E_F;
-            s += exp2f(fmaf(v.x, CUDART_L2E_F, -ml)) + exp2f(fmaf(v.y, CUDART_L2E_F, -ml)) +
-                 exp2f(fmaf(v.z, CUDART_L2E_F, -ml)) + exp2f(fmaf(v.w, CUDART_L2E_F, -ml));
-        }
-        if (part == kLogitCluster - 1) {  // ragged tail of a row whose length is not a multiple of 4
-            for (int j = (n4 << 2) + threadIdx.x; j < V; j += kLsThreads) {
-                float v = x[j];
-                lse_merge(m, s, v, 1.f);
-            }
-        }
-        // warp, then block
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-            float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-            lse_merge(m, s, m2, s2);
-        }
-        const int w = threadIdx.x >> 5;
-        if ((threadIdx.x & 31) == 0) { red_m[w] = m; red_s[w] = s; }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float mm = red_m[0], ss = red_s[0];
-            for (int k = 1; k < kLsThreads / 32; ++k) lse_merge(mm, ss, red_m[k], red_s[k]);
-            part_ms[0] = mm;
-            part_ms[1] = ss;
-        }
-        cluster.sync();
-        // every CTA combines the four partials in the same order
-        float mm = -CUDART_INF_F, ss = 0.f;
-        for (int k = 0; k < kLogitCluster; ++k) {
-            const float* pk = cluster.map_shared_rank(part_ms, k);
-            lse_merge(mm, ss, pk[0], pk[1]);
-        }
-        lse = mm + logf(ss);
-        cluster.sync();  // keep every CTA's shared memory alive until all have read it
+        lse = cluster_row_lse(x, V, cluster, part, red_m, red_s, part_ms);
     } else {
         lse = lse_in[row];
     }
@@ -565,7 +575,75 @@ __global__ void k_set_step(GrState st, int step) {
         if (st.req_step[r] > step) st.req_step[r] = step;
 }
 
+// ---------------------------------------------------------------------------
+// Multi-item scoring: label-token log-probabilities and the ranking
+// ---------------------------------------------------------------------------
+// One cluster per candidate row: log-sum-exp of the full vocabulary, then the label
+// tokens' entries x[label] - LSE (each rounded once).
+__global__ void __cluster_dims__(kLogitCluster, 1, 1) __launch_bounds__(kLsThreads)
+k_label_logprobs(const float* __restrict__ logits, int64_t ld, int vocab, const int32_t* __restrict__ labels,
+                 int n_labels, float* __restrict__ out, int32_t* __restrict__ status) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int row = blockIdx.x / kLogitCluster;
+    const int part = (int)cluster.block_rank();
+    __shared__ float red_m[kLsThreads / 32], red_s[kLsThreads / 32];
+    __shared__ float part_ms[2];
+    const float* x = logits + (int64_t)row * ld;
+    const float lse = cluster_row_lse(x, vocab, cluster, part, red_m, red_s, part_ms);
+    if (part != 0) return;
+    for (int k = threadIdx.x; k < n_labels; k += kLsThreads) {
+        const float lp = __fsub_rn(x[labels[k]], lse);
+        if (lp != lp) atomicOr(status, kStatusNanKey);
+        out[(int64_t)row * n_labels + k] = lp;
+    }
+}
+
+// One CTA per request: its candidates ordered by the first label's log-probability,
+// highest first, ties by candidate index (bitonic sort of (key, ~index) pairs).
+constexpr int kRankThreads = 1024;
+__global__ void __launch_bounds__(kRankThreads) k_rank(const float* __restrict__ lp, int n_labels,
+                                                      const int32_t* __restrict__ cand_off,
+                                                      int32_t* __restrict__ rank_out, int32_t* __restrict__ status) {
+    __shared__ unsigned long long e[kRankThreads];
+    const int r = blockIdx.x;
+    const int c0 = cand_off[r], n = cand_off[r + 1] - c0;
+    const int tid = threadIdx.x;
+    unsigned long long v = 0ull;  // padding sorts last
+    if (tid < n) {
+        float f = lp[(int64_t)(c0 + tid) * n_labels];
+        uint32_t u = 0;
+        if (f != f) atomicOr(status, kStatusNanKey);
+        else u = order_key(f == 0.f ? 0.f : f);
+        v = ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)tid);
+    }
+    e[tid] = v;
+    __syncthreads();
+    for (int k = 2; k <= kRankThreads; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int p = tid ^ j;
+            if (p > tid) {
+                const unsigned long long a = e[tid], b = e[p];
+                if (((tid & k) == 0) ? (a < b) : (a > b)) { e[tid] = b; e[p] = a; }
+            }
+            __syncthreads();
+        }
+    }
+    if (tid < n) rank_out[c0 + tid] = (int32_t)(0xFFFFFFFFu - (uint32_t)(e[tid] & 0xFFFFFFFFull));
+}
+
 }  // namespace
+
+cudaError_t launch_label_logprobs(const float* logits, int64_t ld, int vocab, const int32_t* labels, int n_labels,
+                                  int n_rows, float* out, int32_t* status, cudaStream_t s) {
+    k_label_logprobs<<<n_rows * kLogitCluster, kLsThreads, 0, s>>>(logits, ld, vocab, labels, n_labels, out, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rank(const float* lp, int n_labels, const int32_t* cand_off, int n_req, int32_t* rank_out,
+                        int32_t* status, cudaStream_t s) {
+    k_rank<<<n_req, kRankThreads, 0, s>>>(lp, n_labels, cand_off, rank_out, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_init_state(const GrState& st, cudaStream_t s) {
     k_init_state<<<1, 256, 0, s>>>(st);

@@ -264,6 +264,72 @@ gr_status gr_beam_path(gr_beam* beam, int request, int level, int32_t* parents, 
 gr_status gr_beam_status(gr_beam* beam, int clear_flag, gr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Multi-item candidate scoring                                              */
+/* ------------------------------------------------------------------------ */
+/* "Advancing Generative Recommendation Inference: our collaboration with
+ * NVIDIA on TensorRT LLM", sections "Background: what inference a
+ * recommendation request needs" and "Scoring many candidates at once": the
+ * user prefix and all candidates form one sequence in which each candidate
+ * sees only the prefix and itself; the log-probabilities of label tokens
+ * ("yes" / "no") read at each candidate's last token rank the candidates.
+ * Here the prefix is the request's context in the ContextKV pool (read once
+ * per request on the tensor cores, as in decode) and each candidate token's
+ * other keys are its own candidate's tokens up to itself. */
+typedef struct gr_score gr_score;
+
+typedef struct {
+    int n_layers, n_q_heads, n_kv_heads, head_dim, vocab;   /* as in gr_config */
+    int64_t pool_tokens;       /* tokens per (layer, KV head) in the ContextKV pool */
+    int n_labels;              /* 1..16 label tokens                              */
+    const int32_t* label_ids;  /* host [n_labels], each in [0, vocab); label 0 ranks */
+} gr_score_config;
+
+typedef struct {
+    int64_t ctx_offset;        /* the user prefix in the ContextKV pool           */
+    int ctx_len;               /* >= 1                                            */
+    int n_candidates;          /* 1..1024                                         */
+    const int32_t* seg_lens;   /* host [n_candidates]: tokens of each candidate, 1..16 */
+} gr_score_request;
+
+typedef struct {
+    const void* ctx_k;         /* as in gr_buffers                                */
+    const void* ctx_v;
+    void* seg_k;               /* bf16 [n_layers][rows][n_kv_heads][head_dim]: K of every
+                                  candidate token (row order below); the caller writes it */
+    void* seg_v;               /* same layout                                     */
+    void* workspace;           /* gr_score_workspace_bytes() bytes, 256-byte aligned */
+    size_t workspace_bytes;
+} gr_score_buffers;
+
+/* Rows: the candidate tokens of request 0 (candidate 0's tokens first, in order),
+ * then request 1's, ...; q, out, seg_k and seg_v use this row order.  Candidates
+ * are numbered globally in the same order. */
+gr_status gr_score_workspace_bytes(const gr_score_config* cfg, const gr_score_request* reqs, int n_requests,
+                                   size_t* bytes);
+gr_status gr_score_create(const gr_score_config* cfg, const gr_score_request* reqs, int n_requests,
+                          const gr_score_buffers* bufs, gr_stream_t stream, gr_score** out);
+gr_status gr_score_destroy(gr_score* score);
+/* rows_total = all candidate tokens; row_offsets / cand_offsets (optional,
+ * n_requests+1 ints): first row / first candidate of each request, then the totals. */
+gr_status gr_score_rows(const gr_score* score, int* rows_total, int* row_offsets, int* cand_offsets);
+/* Masked attention of every candidate token at `layer`: each row attends to its
+ * request's prefix and to its own candidate's tokens up to itself.
+ *   q, out  bf16 [rows][n_q_heads][head_dim], 16-byte aligned */
+gr_status gr_score_attn(gr_score* score, int layer, const void* q, void* out, gr_stream_t stream);
+/* Label log-probabilities and the ranking:
+ *   logits    fp32 [n_candidates_total][ld]: row c = the logits at candidate c's
+ *             last token; ld >= vocab, ld % 4 == 0, 16-byte aligned
+ *   logprobs  fp32 [n_candidates_total][n_labels]: x[label] - LSE over the vocabulary
+ *   ranking   int32 [n_candidates_total] (optional): per request, its candidates'
+ *             indices within the request by label 0's log-probability, highest first,
+ *             ties by index */
+gr_status gr_score_labels(gr_score* score, const float* logits, int64_t ld, float* logprobs, int32_t* ranking,
+                          gr_stream_t stream);
+/* Synchronise `stream` and report the device status word (a NaN log-probability
+ * or a timed-out wait); clear_flag != 0 clears it. */
+gr_status gr_score_status(gr_score* score, int clear_flag, gr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Measurement                                                               */
 /* ------------------------------------------------------------------------ */
 
