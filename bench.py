@@ -379,6 +379,7 @@ def run_gpu(args, w):
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, batch) if rank == 0 else None
+    scoring = run_scoring(args, dev) if (rank == 0 and not args.no_scoring) else None
 
     per_kernel = {k: {"launches": n, "ms_per_launch": (t / n if n else 0.0), "ms_per_step": t / args.steps}
                   for k, (n, t) in stats.items() if n}
@@ -408,6 +409,7 @@ def run_gpu(args, w):
                 "cpu_baseline": {"value": 1.0 / cpu_s if cpu_s == cpu_s else None, "unit": "steps/s", "cores": 1,
                                  "kind": "oracle", "sample": sample},
                 "e2e": e2e,
+                "scoring": scoring,
                 "gpu_launches": launches,
                 "clocks": ck}
         print(json.dumps(line), flush=True)
@@ -415,6 +417,67 @@ def run_gpu(args, w):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def run_scoring(args, device):
+    """Multi-item candidate scoring at the pages' scoring size: each call scores 500
+    candidates of one user; a batch of 8 calls with 2,000-token user prefixes and
+    8-token candidates, Qwen3-1.7B attention geometry (28 layers).  One pass = 28
+    masked-attention launches + label log-probs + ranking, inputs resident in HBM."""
+    import torch
+    from beam_decode_gb300 import binding as B
+    NL, Hq, Hkv, D, V = 28, 16, 8, 128, 151936
+    R, n_cand, seg, T = 8, 500, 8, 2000
+    seed = 5
+    shp = (NL, Hkv, R * T, D)
+    ck = torch.empty(shp, dtype=torch.bfloat16, device=device)
+    cv = torch.empty(shp, dtype=torch.bfloat16, device=device)
+    for l in range(NL):
+        ck[l] = wl.device_normal(shp[1:], seed, wl.TAG_CTX_K, device, torch.bfloat16, sub=l)
+        cv[l] = wl.device_normal(shp[1:], seed, wl.TAG_CTX_V, device, torch.bfloat16, sub=l)
+    sc = B.Score(NL, Hq, Hkv, D, V, [9454, 2753], ck, cv, [(r * T, T, [seg] * n_cand) for r in range(R)],
+                 device=device)
+    for l in range(NL):
+        sc.seg_k[l] = wl.device_normal(sc.seg_k.shape[1:], seed, wl.TAG_BEAM_K, device, torch.bfloat16, sub=l)
+        sc.seg_v[l] = wl.device_normal(sc.seg_v.shape[1:], seed, wl.TAG_BEAM_V, device, torch.bfloat16, sub=l)
+    qs = (sc.rows, Hq, D)
+    q = [wl.device_normal(qs, seed, wl.TAG_Q, device, torch.bfloat16, sub=l) for l in range(NL)]
+    out = torch.empty(qs, dtype=torch.bfloat16, device=device)
+    x = wl.device_normal((sc.n_candidates, V), seed, wl.TAG_LOGITS, device, std=2.0)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for l in range(NL):
+            sc.attn(l, q[l], out)
+        return sc.labels(x)
+
+    for _ in range(max(2, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 2)
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    att_ms = 0.0
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # the attention part alone
+    e0.record(stream)
+    for _ in range(steps):
+        for l in range(NL):
+            sc.attn(l, q[l], out)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    att_ms = e0.elapsed_time(e2) / steps
+    if sc.status() != 0:
+        raise RuntimeError("scoring: device status error")
+    flops = 4.0 * NL * Hq * D * R * n_cand * seg * (T + (seg + 1) / 2.0)
+    return {"workload": f"{R} calls x {n_cand} candidates x {seg} tokens, prefix {T}, 28 layers",
+            "calls_per_s": R * 1000.0 / ms, "candidates_per_s": R * n_cand * 1000.0 / ms, "ms_per_pass": ms,
+            "attn_ms_per_layer": att_ms / NL, "attn_TFLOP_s": flops / (att_ms * 1e-3) / 1e12,
+            "labels_ms": ms - att_ms}
 
 
 def run_e2e(args, batch: DeviceBatch):
@@ -497,6 +560,7 @@ def main():
     ap.add_argument("--workload", default="long", choices=["tiny", "page1", "short", "long", "mixed"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a replayed CUDA graph")
+    ap.add_argument("--no-scoring", action="store_true", help="skip the multi-item scoring measurement")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests of the workload (a smaller case for profiling)")
     args = ap.parse_args()
