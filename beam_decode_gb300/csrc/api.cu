@@ -339,8 +339,8 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
                 u.req = r;
                 u.head = h;
                 u.beam0 = ub * bpu;
-                const int rows_left = (reqs[r].beam_width - u.beam0) * G;
-                u.nqt = rows_left > kTileRows ? 2 : 1;
+                const int rows = std::min(bpu, reqs[r].beam_width - u.beam0) * G;  // query rows of this unit
+                u.nqt = (rows + kTileRows - 1) / kTileRows;
                 u.n_tiles = tiles;
                 s.units.push_back(u);
                 total += (int64_t)tiles * u.nqt;
@@ -777,7 +777,7 @@ extern "C" gr_status gr_decode_attn(gr_beam* h, int layer, const void* q, void* 
     }
     const gr_config& c = h->cfg;
     const int G = c.n_q_heads / c.n_kv_heads;
-    CUtensorMap qmap;
+    CUtensorMap qmap;  // 128 query rows per box: 128/G beams x G heads x 64 dimensions
     gr_status s = make_tmap_3d(&qmap, q, c.head_dim, c.n_q_heads, h->rows, (uint64_t)c.head_dim * 2,
                                (uint64_t)c.n_q_heads * c.head_dim * 2, 64, G, kTileRows / G);
     if (s != GR_OK) return s;

@@ -130,9 +130,9 @@ cudaError_t launch_rank(const float* lp, int n_labels, const int32_t* cand_off, 
 
 // ---- launchers (k_attn.cu) ----
 cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes);
-cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
-                            uint16_t* out, int64_t wait_limit_ns, cudaStream_t s);
-cudaError_t launch_score_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
-                              uint16_t* out, int64_t wait_limit_ns, cudaStream_t s);
+cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q, uint16_t* out,
+                            int64_t wait_limit_ns, cudaStream_t s);
+cudaError_t launch_score_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q, uint16_t* out,
+                              int64_t wait_limit_ns, cudaStream_t s);
 
 }  // namespace grb

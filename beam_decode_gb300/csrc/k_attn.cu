@@ -15,8 +15,9 @@
 // k_ctx_attn (per CTA: a list of jobs = key-tile ranges of 256-row units)
 //   warp 0     TMA producer: Q tiles once per job, then K and V tiles of 128
 //              keys through a two-stage shared-memory ring (128-byte swizzle).
-//   warp 1     MMA issuer (one thread): S_i = Q_i K^T into TMEM (M=128, N=128,
-//              K=16 per instruction), O_i += P_i V with P_i read from TMEM.
+//   warps 1, 3 MMA issuers (one thread each): warp 3 issues S_i = Q_i K^T into
+//              TMEM (M=128, N=128, K=16 per instruction), warp 1 issues
+//              O_i += P_i V with P_i read from TMEM.
 //   warp 2     TMEM allocation (512 columns: S0, S1, O0, O1).
 //   warps 4-7  softmax of query tile 0; warps 8-11 softmax of query tile 1:
 //              one thread per row (TMEM lane), online max/sum with a lazy
@@ -344,7 +345,7 @@ struct Plan {
 
 enum Bar {
     B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = 4, B_V_FULL = 6, B_V_EMPTY = 8,
-    B_S_FULL = 10, B_P_FULL = 12, B_O_FULL = 14, B_O_EMPTY = 16, B_DRAIN = 18, B_COUNT = 19
+    B_S_FULL = 10, B_P_FULL = 12, B_O_FULL = 14, B_O_EMPTY = 16, B_DRAIN = 18, B_PVD = 20, B_COUNT = 22
 };
 
 constexpr int kAttnThreads = 384;
@@ -378,7 +379,10 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             mbar_init(bar(B_O_FULL + s), 1);
             mbar_init(bar(B_O_EMPTY + s), 128);
         }
-        mbar_init(bar(B_DRAIN), 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bar(B_DRAIN + k), 1);
+            mbar_init(bar(B_PVD + k), 1);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -441,91 +445,91 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 3) {
+        // Two MMA issuers (one thread each): warp 3 issues S_i = Q_i K^T, warp 1 issues
+        // O_i += P_i V.  S_i of key tile j overwrites P_i of tile j-1, so it waits until
+        // that PV has completed (B_PVD + i).  Each thread's waits and commits then overlap
+        // the other's MMAs, which keeps the tensor pipe fed.
         if (lane == 0) {
             bool mma_issued = false;
-            constexpr uint32_t idesc_s = idesc_bf16(128, kTileKeys, false);
-            constexpr uint32_t idesc_o = idesc_bf16(128, D, true);
-            uint32_t kit = 0, vit = 0, qcnt = 0;
-            uint32_t tiles[2] = {0, 0}, jobs_i[2] = {0, 0};
             bool ok = true;
-            auto issue_s = [&](int i, int ks) {
-                const uint32_t d = tmem + P::s_col(i);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * P::kBoxBytes + (kk & 3) * 32;
-                    const uint64_t a = smem_desc(sb + P::kQOff + i * P::kQTile + off, 16, 1024);
-                    const uint64_t b = smem_desc(sb + P::kKOff + ks * P::kKVTile + off, 16, 1024);
-                    mma_ss(d, a, b, idesc_s, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int i, int vs, bool acc) {
-                const uint32_t d = tmem + P::o_col(i);
-#pragma unroll
-                for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-                    const uint32_t a = tmem + P::p_col(i) + kk * 8;
-                    const uint64_t b = smem_desc(sb + P::kVOff + vs * P::kKVTile + kk * 16 * 128, P::kBoxBytes, 1024);
-                    mma_ts(d, a, b, idesc_o, (acc || kk > 0) ? 1u : 0u);
-                }
-            };
-            for (int jb = jr.x; jb < jr.y && ok; ++jb) {
-                const GrAttnJob J = st.jobs[jb];
-                const GrAttnUnit U = st.units[J.unit];
-                if (!decoding<kScore>(st, U)) continue;
-                const int nqt = U.nqt;
-                const int n = J.t1 - J.t0;
-                if (!(ok = wait1(bar(B_Q_FULL), qcnt & 1, wt))) break;
-                ++qcnt;
-                int ks = kit & 1;
-                if (!(ok = wait1(bar(B_K_FULL + ks), (kit >> 1) & 1, wt))) break;
-                tc_fence_after();
-                for (int i = 0; i < nqt; ++i) {
-                    issue_s(i, ks);
-                    tc_commit(bar(B_S_FULL + i));
-                }
-                mma_issued = true;
-                tc_commit(bar(B_K_EMPTY + ks));
-                ++kit;
-                if (n == 1) tc_commit(bar(B_Q_EMPTY));
-                for (int jj = 0; jj < n && ok; ++jj) {
-                    const int vs = vit & 1;
-                    if (!(ok = wait1(bar(B_V_FULL + vs), (vit >> 1) & 1, wt))) break;
-                    for (int i = 0; i < nqt; ++i) {
-                        if (!(ok = wait1(bar(B_P_FULL + i), tiles[i] & 1, wt))) break;
-                        tc_fence_after();
-                        if (jj == 0 && jobs_i[i] > 0) {
-                            if (!(ok = wait1(bar(B_O_EMPTY + i), (jobs_i[i] - 1) & 1, wt))) break;
+            if (warp == 3) {
+                constexpr uint32_t idesc_s = idesc_bf16(128, kTileKeys, false);
+                uint32_t kit = 0, qcnt = 0, s_i[2] = {0, 0};
+                for (int jb = jr.x; jb < jr.y && ok; ++jb) {
+                    const GrAttnJob J = st.jobs[jb];
+                    const GrAttnUnit U = st.units[J.unit];
+                    if (!decoding<kScore>(st, U)) continue;
+                    const int nqt = U.nqt;
+                    const int n = J.t1 - J.t0;
+                    if (!(ok = wait1(bar(B_Q_FULL), qcnt & 1, wt))) break;
+                    ++qcnt;
+                    for (int jj = 0; jj < n && ok; ++jj) {
+                        const int ks = kit & 1;
+                        if (!(ok = wait1(bar(B_K_FULL + ks), (kit >> 1) & 1, wt))) break;
+                        for (int i = 0; i < nqt; ++i) {
+                            if (s_i[i] > 0 && !(ok = wait1(bar(B_PVD + i), (s_i[i] - 1) & 1, wt))) break;
                             tc_fence_after();
-                        }
-                        issue_pv(i, vs, jj > 0);
-                        ++tiles[i];
-                        if (jj == n - 1) {
-                            tc_commit(bar(B_O_FULL + i));
-                        } else {
-                            if (i == 0) {
-                                ks = kit & 1;
-                                if (!(ok = wait1(bar(B_K_FULL + ks), (kit >> 1) & 1, wt))) break;
-                                tc_fence_after();
+                            const uint32_t d = tmem + P::s_col(i);
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk >> 2) * P::kBoxBytes + (kk & 3) * 32;
+                                const uint64_t a = smem_desc(sb + P::kQOff + i * P::kQTile + off, 16, 1024);
+                                const uint64_t b = smem_desc(sb + P::kKOff + ks * P::kKVTile + off, 16, 1024);
+                                mma_ss(d, a, b, idesc_s, kk > 0 ? 1u : 0u);
                             }
-                            issue_s(i, ks);
+                            mma_issued = true;
                             tc_commit(bar(B_S_FULL + i));
-                            if (i == nqt - 1) {
-                                tc_commit(bar(B_K_EMPTY + ks));
-                                ++kit;
-                                if (jj + 1 == n - 1) tc_commit(bar(B_Q_EMPTY));
-                            }
+                            ++s_i[i];
                         }
+                        if (!ok) break;
+                        tc_commit(bar(B_K_EMPTY + ks));
+                        ++kit;
+                        if (jj == n - 1) tc_commit(bar(B_Q_EMPTY));
                     }
-                    if (!ok) break;
-                    tc_commit(bar(B_V_EMPTY + vs));
-                    ++vit;
                 }
-                for (int i = 0; i < nqt; ++i) ++jobs_i[i];
+            } else {
+                constexpr uint32_t idesc_o = idesc_bf16(128, D, true);
+                uint32_t vit = 0, pv_i[2] = {0, 0}, jobs_i[2] = {0, 0};
+                for (int jb = jr.x; jb < jr.y && ok; ++jb) {
+                    const GrAttnJob J = st.jobs[jb];
+                    const GrAttnUnit U = st.units[J.unit];
+                    if (!decoding<kScore>(st, U)) continue;
+                    const int nqt = U.nqt;
+                    const int n = J.t1 - J.t0;
+                    for (int jj = 0; jj < n && ok; ++jj) {
+                        const int vs = vit & 1;
+                        if (!(ok = wait1(bar(B_V_FULL + vs), (vit >> 1) & 1, wt))) break;
+                        for (int i = 0; i < nqt; ++i) {
+                            if (!(ok = wait1(bar(B_P_FULL + i), pv_i[i] & 1, wt))) break;
+                            if (jj == 0 && jobs_i[i] > 0 && !(ok = wait1(bar(B_O_EMPTY + i), (jobs_i[i] - 1) & 1, wt)))
+                                break;
+                            tc_fence_after();
+                            const uint32_t d = tmem + P::o_col(i);
+#pragma unroll
+                            for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+                                const uint32_t a = tmem + P::p_col(i) + kk * 8;
+                                const uint64_t b =
+                                    smem_desc(sb + P::kVOff + vs * P::kKVTile + kk * 16 * 128, P::kBoxBytes, 1024);
+                                mma_ts(d, a, b, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            mma_issued = true;
+                            tc_commit(bar(B_PVD + i));  // S_i of the next tile may overwrite P_i
+                            ++pv_i[i];
+                            if (jj == n - 1) tc_commit(bar(B_O_FULL + i));
+                        }
+                        if (!ok) break;
+                        tc_commit(bar(B_V_EMPTY + vs));
+                        ++vit;
+                    }
+                    for (int i = 0; i < nqt; ++i) ++jobs_i[i];
+                }
             }
             // all issued tensor-core work (and its commits) completes before TMEM is freed
             if (mma_issued) {
-                tc_commit(bar(B_DRAIN));
-                wait_drain(bar(B_DRAIN), 0);
+                const int dr = B_DRAIN + (warp == 3 ? 1 : 0);
+                tc_commit(bar(dr));
+                wait_drain(bar(dr), 0);
             }
         }
         __syncwarp();
