@@ -744,10 +744,10 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 if (staged) {
                     // lanes split each of the warp's rows: coalesced loads, shuffle reduction
                     constexpr int E = D / 32;
-                    for (int r0 = 0; r0 < 32; r0 += 8) {
-                        float dsum[8];
+                    for (int r0 = 0; r0 < 32; r0 += 16) {  // 16 rows' loads in flight per batch
+                        float dsum[16];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
+                        for (int k = 0; k < 16; ++k) {
                             const uint16_t* qp = reinterpret_cast<const uint16_t*>(
                                 __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(qp_mine), r0 + k));
                             const uint16_t* kp = reinterpret_cast<const uint16_t*>(
@@ -769,7 +769,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                             dsum[k] = d;
                         }
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
+                        for (int k = 0; k < 16; ++k) {
                             float d = dsum[k];
 #pragma unroll
                             for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
@@ -794,13 +794,28 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 }
                 sj[j] = j < n_priv ? mine * scale : -CUDART_INF_F;
             }
-            // ---- weights of the parts (own piece, published pieces, beam tokens)
+            // ---- weights of the parts (own piece, published pieces, beam tokens); the
+            // pieces' log-sum-exps are loaded once, all in flight together
+            constexpr int kPieceRegs = 4;
             const float* lse_col = st.lse_part + (int64_t)U.first_slot * kUnitRows + prow;
+            float wp[kPieceRegs];
+#pragma unroll
+            for (int pp = 0; pp < kPieceRegs; ++pp)
+                wp[pp] = (live && pp < n_other) ? __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) : -CUDART_INF_F;
             float M = lse_own;
-            for (int pp = 1; pp <= n_other; ++pp) M = fmaxf(M, __ldcg(lse_col + (int64_t)pp * kUnitRows));
+#pragma unroll
+            for (int pp = 0; pp < kPieceRegs; ++pp) M = fmaxf(M, wp[pp]);
+            for (int pp = kPieceRegs + 1; live && pp <= n_other; ++pp)
+                M = fmaxf(M, __ldcg(lse_col + (int64_t)pp * kUnitRows));
             for (int j = 0; j < t_w; ++j) M = fmaxf(M, sj[j]);
             float den = __expf(lse_own - M);
-            for (int pp = 1; pp <= n_other; ++pp) den += __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
+#pragma unroll
+            for (int pp = 0; pp < kPieceRegs; ++pp) {
+                wp[pp] = pp < n_other ? __expf(wp[pp] - M) : 0.f;  // now the unnormalised weight
+                den += wp[pp];
+            }
+            for (int pp = kPieceRegs + 1; live && pp <= n_other; ++pp)
+                den += __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
             float w_j[kMaxPriv];
             for (int j = 0; j < t_w; ++j) { w_j[j] = __expf(sj[j] - M); den += w_j[j]; }
             // dead beams come out as exact zeros: none of their (unwritten) inputs is used
@@ -810,17 +825,23 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             float* a = reinterpret_cast<float*>(ov);  // the row accumulates in place of O
 #pragma unroll
             for (int c = 0; c < D; ++c) a[c] = live ? __uint_as_float(ov[c]) * c_own : 0.f;
-            // ---- published pieces: column-major, coalesced across the warp
+            // ---- published pieces: column-major (coalesced across the warp), 64 columns
+            // per batch of loads
             for (int pp = 1; live && pp <= n_other; ++pp) {
-                const float w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M) * inv_den;
+                float w = 0.f;
+#pragma unroll
+                for (int k = 0; k < kPieceRegs; ++k) w = (k == pp - 1) ? wp[k] : w;
+                if (pp > kPieceRegs) w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
+                w *= inv_den;
                 const float* op = st.o_part + (int64_t)(U.first_slot + pp) * D * kUnitRows + prow;
+                constexpr int kBatch = D < 64 ? D : 64;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float x[32];
+                for (int c0 = 0; c0 < D; c0 += kBatch) {
+                    float x[kBatch];
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) x[u] = __ldcg(op + (int64_t)(c0 + u) * kUnitRows);
+                    for (int u = 0; u < kBatch; ++u) x[u] = __ldcg(op + (int64_t)(c0 + u) * kUnitRows);
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) a[c0 + u] = fmaf(w, x[u], a[c0 + u]);
+                    for (int u = 0; u < kBatch; ++u) a[c0 + u] = fmaf(w, x[u], a[c0 + u]);
                 }
                 st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
             }
@@ -830,12 +851,19 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                     const uint16_t* vp_mine = st.beam_v + (live ? kvj[j] : 0) * D;
                     __syncwarp();
                     constexpr int kRowsPer = 32 / kChunks;  // rows one warp instruction covers
-                    for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
-                        const int r = r0 + lane / kChunks, c = lane % kChunks;
+                    constexpr int kIters = 32 / kRowsPer;
+                    uint4 vt[kIters];  // every load in flight before the first store
+#pragma unroll
+                    for (int it = 0; it < kIters; ++it) {
+                        const int r = it * kRowsPer + lane / kChunks, c = lane % kChunks;
                         const uint16_t* vp = reinterpret_cast<const uint16_t*>(
                             __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(vp_mine), r));
-                        const uint4 v = __ldg(reinterpret_cast<const uint4*>(vp) + c);
-                        *reinterpret_cast<uint4*>(stg + (r * kChunks + (c ^ (r & (kChunks - 1)))) * 16) = v;
+                        vt[it] = __ldg(reinterpret_cast<const uint4*>(vp) + c);
+                    }
+#pragma unroll
+                    for (int it = 0; it < kIters; ++it) {
+                        const int r = it * kRowsPer + lane / kChunks, c = lane % kChunks;
+                        *reinterpret_cast<uint4*>(stg + (r * kChunks + (c ^ (r & (kChunks - 1)))) * 16) = vt[it];
                     }
                     __syncwarp();
 #pragma unroll
