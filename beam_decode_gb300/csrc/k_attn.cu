@@ -94,6 +94,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
         "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// untiled bulk copy global -> shared, completion counted on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16 bytes)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void tmap_acquire(const void* tmap) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmap) : "memory");
 }
@@ -221,10 +228,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -322,6 +325,48 @@ __device__ __forceinline__ bool decoding(const GrState& st, const GrAttnUnit& U)
 }
 
 // ---------------------------------------------------------------------------
+// one query row of a unit, as a softmax thread (TMEM lane) sees it
+// ---------------------------------------------------------------------------
+struct RowInfo {
+    int b;                 // beam (decode) / candidate-token row (scoring) within the request
+    bool row_ok;           // the row exists (b < W_r)
+    bool live;             // and takes part: an alive beam / a scored token
+    int n_priv;            // private keys: decode t (levels 0..t-1 of BeamKV), scoring pos + 1
+    int pool0;             // scoring: pool row of the segment's first token
+    int64_t orow_idx;      // query / output row (row x query head)
+    const int32_t* path;   // decode: the beam's ancestry row at level t-1
+};
+
+template <bool kScore>
+__device__ __forceinline__ RowInfo row_info(const GrState& st, const GrAttnUnit& U, int i, int row_t, int G) {
+    RowInfo ri;
+    const GrReqDev& R = st.req[U.req];
+    const int t = kScore ? 0 : st.req_step[U.req];
+    ri.b = U.beam0 + i * (kTileRows / G) + row_t / G;
+    const int g = row_t % G;
+    ri.row_ok = ri.b < R.width;
+    ri.live = ri.row_ok && (kScore || ri.b < st.n_beams[U.req * (st.n_levels + 1) + t]);
+    ri.orow_idx = (int64_t)(R.row_off + ri.b) * st.n_q_heads + U.head * G + g;
+    ri.pool0 = 0;
+    ri.path = nullptr;
+    ri.n_priv = 0;
+    if constexpr (kScore) {
+        if (ri.live) {
+            ri.n_priv = st.seg_pos[R.row_off + ri.b] + 1;
+            ri.pool0 = st.seg_first[R.row_off + ri.b];
+        }
+    } else {
+        ri.n_priv = ri.live ? t : 0;
+        ri.path = st.path + ((int64_t)(t - 1) * st.rows + R.row_off + ri.b) * st.n_levels;
+    }
+    return ri;
+}
+
+// bf16 pair -> two floats
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
 // shared-memory plan
 // ---------------------------------------------------------------------------
 template <int D>
@@ -345,7 +390,9 @@ struct Plan {
 
 enum Bar {
     B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = 4, B_V_FULL = 6, B_V_EMPTY = 8,
-    B_S_FULL = 10, B_P_FULL = 12, B_O_FULL = 14, B_O_EMPTY = 16, B_DRAIN = 18, B_PVD = 20, B_COUNT = 22
+    B_S_FULL = 10, B_P_FULL = 12, B_O_FULL = 14, B_O_EMPTY = 16, B_DRAIN = 18, B_PVD = 20,
+    B_BEAM = 22,  // one per softmax warp: its BeamKV rows copied into the freed rings
+    B_COUNT = 30
 };
 
 constexpr int kAttnThreads = 384;
@@ -383,6 +430,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             mbar_init(bar(B_DRAIN + k), 1);
             mbar_init(bar(B_PVD + k), 1);
         }
+        for (int k = 0; k < 8; ++k) mbar_init(bar(B_BEAM + k), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -556,51 +604,33 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
     regs_inc<224>();
     {
         // softmax warpgroups
-        const int i = (warp - 4) >> 2;          // query tile of this warpgroup
-        const int quarter = warp & 3;           // TMEM lane quarter
-        const int row_t = quarter * 32 + lane;  // row within the tile
+        const int i = (warp - 4) >> 2;           // query tile of this warpgroup
+        const int quarter = warp & 3;            // TMEM lane quarter
+        const int row_t = quarter * 32 + lane;   // row within the tile
+        const int prow = i * kTileRows + row_t;  // row within the unit
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        uint32_t tiles = 0, jobs = 0;
+        uint32_t tiles = 0, jobs = 0, ktiles = 0, bcnt = 0;
         bool ok = true;
+        // A published piece's ready flag is raised when the next job starts (or at the end),
+        // after that job's row set-up: by then its stores have drained and the release fence
+        // costs little.
+        uint32_t* pend_flag = nullptr;
         for (int jb = jr.x; jb < jr.y && ok; ++jb) {
             const GrAttnJob J = st.jobs[jb];
             const GrAttnUnit U = st.units[J.unit];
-            if (i >= U.nqt || !decoding<kScore>(st, U)) continue;
-            const int t = kScore ? 0 : st.req_step[U.req];  // decode: 1 <= t < L_r, BeamKV levels 0..t-1
-            const int ctx_len = st.req[U.req].ctx_len;
+            if (!decoding<kScore>(st, U)) continue;
             const int n = J.t1 - J.t0;
+            ktiles += n;  // key tiles the S issuer has taken through the K ring so far
+            if (i >= U.nqt) continue;
+            const RowInfo ri = row_info<kScore>(st, U, i, row_t, G);
+            const int ctx_len = st.req[U.req].ctx_len;
             const bool merger = (J.slot == U.first_slot);
-            // this row's beam and query head
-            const GrReqDev& R = st.req[U.req];
-            const int b = U.beam0 + i * (kTileRows / G) + row_t / G;
-            const int g = row_t % G;
-            const bool row_ok = b < R.width;
-            const bool live = row_ok && (kScore || b < st.n_beams[U.req * (st.n_levels + 1) + t]);
-            const int64_t orow_idx = (int64_t)(R.row_off + b) * st.n_q_heads + U.head * G + g;
-            const int L = st.n_levels;
-            // The row's private keys.  Decode: the t BeamKV tokens on the beam's path, one per
-            // level, found through its ancestry row.  Scoring: the tokens of the row's own
-            // candidate up to itself.  The warp's loops run to t_w (the largest count of its
-            // rows); a row's surplus keys read row 0 of the pool and get weight 0.
-            const int32_t* path = kScore ? nullptr : st.path + ((int64_t)(t - 1) * st.rows + R.row_off + b) * L;
-            int n_priv = 0, seg0 = 0;
-            if constexpr (kScore) {
-                if (live) {
-                    n_priv = st.seg_pos[R.row_off + b] + 1;
-                    seg0 = st.seg_first[R.row_off + b];
-                }
-            } else {
-                n_priv = live ? t : 0;
-                if (merger && live) prefetch_l2(path);
+            if (pend_flag != nullptr) {
+                // the previous job's piece: its stores have drained by now, so the fence is cheap
+                __threadfence();
+                *reinterpret_cast<volatile uint32_t*>(pend_flag) = 1u;
+                pend_flag = nullptr;
             }
-            const int t_w = kScore ? __reduce_max_sync(0xffffffffu, n_priv) : t;
-            auto priv_row = [&](int j) -> int64_t {
-                if (j >= n_priv) return 0;
-                if constexpr (kScore) return ((int64_t)layer * st.rows + seg0 + j) * st.n_kv_heads + U.head;
-                return (((int64_t)layer * (L - 1) + j) * st.rows + R.row_off + path[j]) * st.n_kv_heads + U.head;
-            };
-            const int jj_pf = n > 2 ? n - 2 : 0;  // tile at which the merge inputs are prefetched
-            int64_t kvj[kMaxPriv];
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int jj = 0; jj < n; ++jj) {
                 if (!(ok = wait_warp(bar(B_S_FULL + i), tiles & 1, wt))) break;
@@ -669,24 +699,6 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 tc_fence_before();
                 mbar_arrive(bar(B_P_FULL + i));
                 ++tiles;
-                if (merger && jj == jj_pf) {
-                    // two tiles before the merge: pull its inputs into L2 (ancestry-indexed
-                    // BeamKV rows, the query row, the published pieces' columns)
-                    if (live) {
-                        const char* qrow = reinterpret_cast<const char*>(q + orow_idx * D);
-                        for (int o = 0; o < D * 2; o += 128) prefetch_l2(qrow + o);
-                        for (int j = 0; j < n_priv; ++j) {
-                            kvj[j] = priv_row(j);
-                            const char* kr = reinterpret_cast<const char*>(st.beam_k + kvj[j] * D);
-                            const char* vr = reinterpret_cast<const char*>(st.beam_v + kvj[j] * D);
-                            for (int o = 0; o < D * 2; o += 128) { prefetch_l2(kr + o); prefetch_l2(vr + o); }
-                        }
-                    }
-                    const int prow_w = i * kTileRows + quarter * 32;  // the warp's 32 rows share a line per column
-                    for (int pp = 1; pp < U.n_slots; ++pp)
-                        for (int c = lane; c < D; c += 32)
-                            prefetch_l2(st.o_part + ((int64_t)(U.first_slot + pp) * D + c) * kUnitRows + prow_w);
-                }
             }
             if (!ok) break;
             // epilogue
@@ -694,230 +706,259 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             tc_fence_after();
             const float lse_own = m_used * scale + logf(l);
             const float inv_l = 1.f / l;
-            const int prow = i * kTileRows + row_t;
             uint32_t ov[D];  // this piece's unnormalised O row
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_base + P::o_col(i) + 32 * c, ov + 32 * c);
             tc_fence_before();
             mbar_arrive(bar(B_O_EMPTY + i));  // TMEM O is free for the next job
             ++jobs;
-            const int piece = J.slot - U.first_slot;
-            if (piece != 0) {
+            if (!merger) {
                 // a later key range of a split unit: publish the normalised piece and its
-                // log-sum-exp, then this row's ready flag; the merger clears the flag once it
-                // has read the row, so flags need no per-launch tag and a captured step replays.
-                // Only live rows are published (the merger reads no other row).
-                // Column-major piece [slot][D][256 rows]: a warp stores 32 consecutive rows of
-                // one column per instruction (one 128-byte transaction).
-                if (live) {
-                    float* ocol = st.o_part + (int64_t)J.slot * D * kUnitRows + prow;
+                // log-sum-exp; the ready flag follows (see pend_flag).  The merger clears the
+                // flag once it has read the row, so flags need no per-launch tag and a
+                // captured step replays.  Only live rows are published (the merger reads no
+                // other row).  Layout [slot][D/4][256 rows][4]: a warp stores 32 consecutive
+                // rows' 16-byte chunks of one column group per instruction (512 bytes).
+                if (ri.live) {
+                    float4* dst = reinterpret_cast<float4*>(st.o_part) + (int64_t)J.slot * (D / 4) * kUnitRows + prow;
 #pragma unroll
-                    for (int c = 0; c < D; ++c) __stcg(ocol + (int64_t)c * kUnitRows, __uint_as_float(ov[c]) * inv_l);
+                    for (int c = 0; c < D / 4; ++c)
+                        __stcg(dst + (int64_t)c * kUnitRows,
+                               make_float4(__uint_as_float(ov[4 * c]) * inv_l, __uint_as_float(ov[4 * c + 1]) * inv_l,
+                                           __uint_as_float(ov[4 * c + 2]) * inv_l, __uint_as_float(ov[4 * c + 3]) * inv_l));
                     __stcg(st.lse_part + (int64_t)J.slot * kUnitRows + prow, lse_own);
-                    __threadfence();
-                    *reinterpret_cast<volatile uint32_t*>(st.piece_flag + (int64_t)J.slot * kUnitRows + prow) = 1u;
+                    pend_flag = st.piece_flag + (int64_t)J.slot * kUnitRows + prow;
                 }
                 continue;
             }
-            // the first key range merges: the other pieces of the unit (finished earlier,
-            // at the start of their CTAs' ranges) and the beam's BeamKV tokens.  When this
-            // is the CTA's last job every S MMA has completed and nothing more is loaded, so
-            // the warp's 32 rows of V and of output pass through its share of the K stages
-            // and are read / written coalesced; otherwise thread by thread.
+            // The first key range merges, by a log-sum-exp combine: its own O (registers),
+            // the other pieces (finished earlier, at the start of their CTAs' ranges) and the
+            // beam part -- the row's private keys (decode: the t BeamKV tokens on its beam's
+            // ancestry path; scoring: its own candidate up to itself), folded in one key at a
+            // time with an online max.  Each thread works on its own row.  When this is the
+            // CTA's last job, the K and V rings are free once the last key tile's MMAs have
+            // completed: each warp copies the private keys' K and V rows of its 32 rows there
+            // (bulk copies, 31 key slots at a time), reads q from the job's Q tile, and
+            // finally passes its bf16 output rows through the same space to write them
+            // coalesced.  Otherwise every row reads q, K and V from global memory.
             const bool staged = (jb == jr.y - 1);
-            constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per bf16 row
-            uint8_t* stg = smem + P::kKOff + (warp - 4) * 32 * D * 2;
             const int n_other = U.n_slots - 1;
             bool have = true;
-            if (live)
+            if (ri.live)
                 for (int pp = 1; pp <= n_other && have; ++pp)
                     have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, 1u, wt);
             if (__any_sync(0xffffffffu, !have)) { ok = false; break; }
             __threadfence();
-            // ---- beam scores q . k_j / sqrt(D)
-            float sj[kMaxPriv];
-            for (int j = 0; j < t_w; ++j) {
-                kvj[j] = priv_row(j);
-                const uint16_t* qp_mine = q + (live ? orow_idx : 0) * D;
-                const uint16_t* kp_mine = st.beam_k + (live ? kvj[j] : 0) * D;
-                float mine = 0.f;
-                if (staged) {
-                    // lanes split each of the warp's rows: coalesced loads, shuffle reduction
-                    constexpr int E = D / 32;
-                    for (int r0 = 0; r0 < 32; r0 += 16) {  // 16 rows' loads in flight per batch
-                        float dsum[16];
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const uint16_t* qp = reinterpret_cast<const uint16_t*>(
-                                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(qp_mine), r0 + k));
-                            const uint16_t* kp = reinterpret_cast<const uint16_t*>(
-                                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(kp_mine), r0 + k));
-                            float d = 0.f;
-                            if constexpr (E == 4) {
-                                const uint2 qa = __ldg(reinterpret_cast<const uint2*>(qp) + lane);
-                                const uint2 ka = __ldg(reinterpret_cast<const uint2*>(kp) + lane);
-                                d = __uint_as_float(qa.x << 16) * __uint_as_float(ka.x << 16) +
-                                    __uint_as_float(qa.x & 0xFFFF0000u) * __uint_as_float(ka.x & 0xFFFF0000u) +
-                                    __uint_as_float(qa.y << 16) * __uint_as_float(ka.y << 16) +
-                                    __uint_as_float(qa.y & 0xFFFF0000u) * __uint_as_float(ka.y & 0xFFFF0000u);
-                            } else {
-                                const uint32_t qa = __ldg(reinterpret_cast<const uint32_t*>(qp) + lane);
-                                const uint32_t ka = __ldg(reinterpret_cast<const uint32_t*>(kp) + lane);
-                                d = __uint_as_float(qa << 16) * __uint_as_float(ka << 16) +
-                                    __uint_as_float(qa & 0xFFFF0000u) * __uint_as_float(ka & 0xFFFF0000u);
-                            }
-                            dsum[k] = d;
-                        }
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            float d = dsum[k];
-#pragma unroll
-                            for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-                            if (lane == r0 + k) mine = d;
-                        }
-                    }
-                } else if (live) {
-                    const uint4* qrow = reinterpret_cast<const uint4*>(qp_mine);
-                    const uint4* krow = reinterpret_cast<const uint4*>(kp_mine);
-                    float d0 = 0.f, d1 = 0.f;
-#pragma unroll 4
-                    for (int e = 0; e < D / 8; ++e) {
-                        const uint4 qa = __ldg(qrow + e), ka = __ldg(krow + e);
-                        const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
-#pragma unroll
-                        for (int h2 = 0; h2 < 4; ++h2) {
-                            d0 = fmaf(__uint_as_float(qw[h2] << 16), __uint_as_float(kw[h2] << 16), d0);
-                            d1 = fmaf(__uint_as_float(qw[h2] & 0xFFFF0000u), __uint_as_float(kw[h2] & 0xFFFF0000u), d1);
-                        }
-                    }
-                    mine = d0 + d1;
-                }
-                sj[j] = j < n_priv ? mine * scale : -CUDART_INF_F;
-            }
-            // ---- weights of the parts (own piece, published pieces, beam tokens); the
-            // pieces' log-sum-exps are loaded once, all in flight together
+            // ---- the context part: own O and the published pieces, relative to the max M of
+            // their log-sum-exps; a and den stay unnormalised until the end
             constexpr int kPieceRegs = 4;
             const float* lse_col = st.lse_part + (int64_t)U.first_slot * kUnitRows + prow;
             float wp[kPieceRegs];
 #pragma unroll
             for (int pp = 0; pp < kPieceRegs; ++pp)
-                wp[pp] = (live && pp < n_other) ? __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) : -CUDART_INF_F;
+                wp[pp] = (ri.live && pp < n_other) ? __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) : -CUDART_INF_F;
             float M = lse_own;
 #pragma unroll
             for (int pp = 0; pp < kPieceRegs; ++pp) M = fmaxf(M, wp[pp]);
-            for (int pp = kPieceRegs + 1; live && pp <= n_other; ++pp)
+            for (int pp = kPieceRegs + 1; ri.live && pp <= n_other; ++pp)
                 M = fmaxf(M, __ldcg(lse_col + (int64_t)pp * kUnitRows));
-            for (int j = 0; j < t_w; ++j) M = fmaxf(M, sj[j]);
-            float den = __expf(lse_own - M);
+            const float w_own = __expf(lse_own - M);
+            float den = w_own;
 #pragma unroll
             for (int pp = 0; pp < kPieceRegs; ++pp) {
-                wp[pp] = pp < n_other ? __expf(wp[pp] - M) : 0.f;  // now the unnormalised weight
+                wp[pp] = pp < n_other ? __expf(wp[pp] - M) : 0.f;
                 den += wp[pp];
             }
-            for (int pp = kPieceRegs + 1; live && pp <= n_other; ++pp)
-                den += __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
-            float w_j[kMaxPriv];
-            for (int j = 0; j < t_w; ++j) { w_j[j] = __expf(sj[j] - M); den += w_j[j]; }
-            // dead beams come out as exact zeros: none of their (unwritten) inputs is used
-            const float inv_den = 1.f / den;
-            const float c_own = live ? __expf(lse_own - M) * inv_l * inv_den : 0.f;
-            for (int j = 0; j < t_w; ++j) w_j[j] = live ? w_j[j] * inv_den : 0.f;
             float* a = reinterpret_cast<float*>(ov);  // the row accumulates in place of O
+            {
+                const float c_own = ri.live ? w_own * inv_l : 0.f;
 #pragma unroll
-            for (int c = 0; c < D; ++c) a[c] = live ? __uint_as_float(ov[c]) * c_own : 0.f;
-            // ---- published pieces: column-major (coalesced across the warp), 64 columns
-            // per batch of loads
-            for (int pp = 1; live && pp <= n_other; ++pp) {
+                for (int c = 0; c < D; ++c) a[c] = ri.live ? __uint_as_float(ov[c]) * c_own : 0.f;
+            }
+#pragma unroll 1
+            for (int pp = 1; ri.live && pp <= n_other; ++pp) {
                 float w = 0.f;
 #pragma unroll
                 for (int k = 0; k < kPieceRegs; ++k) w = (k == pp - 1) ? wp[k] : w;
-                if (pp > kPieceRegs) w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
-                w *= inv_den;
-                const float* op = st.o_part + (int64_t)(U.first_slot + pp) * D * kUnitRows + prow;
-                constexpr int kBatch = D < 64 ? D : 64;
+                if (pp > kPieceRegs) {
+                    w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
+                    den += w;
+                }
+                const float4* src =
+                    reinterpret_cast<const float4*>(st.o_part) + (int64_t)(U.first_slot + pp) * (D / 4) * kUnitRows + prow;
+                constexpr int kBatch = D / 16;  // chunks per batch of loads
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += kBatch) {
-                    float x[kBatch];
+                for (int c0 = 0; c0 < D / 4; c0 += kBatch) {
+                    float4 x[kBatch];
 #pragma unroll
-                    for (int u = 0; u < kBatch; ++u) x[u] = __ldcg(op + (int64_t)(c0 + u) * kUnitRows);
+                    for (int u = 0; u < kBatch; ++u) x[u] = __ldcg(src + (int64_t)(c0 + u) * kUnitRows);
 #pragma unroll
-                    for (int u = 0; u < kBatch; ++u) a[c0 + u] = fmaf(w, x[u], a[c0 + u]);
+                    for (int u = 0; u < kBatch; ++u) {
+                        float* ac = a + 4 * (c0 + u);
+                        ac[0] = fmaf(w, x[u].x, ac[0]);
+                        ac[1] = fmaf(w, x[u].y, ac[1]);
+                        ac[2] = fmaf(w, x[u].z, ac[2]);
+                        ac[3] = fmaf(w, x[u].w, ac[3]);
+                    }
                 }
                 st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
             }
-            // ---- BeamKV values (scoring: the candidate's own values)
-            for (int j = 0; j < t_w; ++j) {
-                if (staged) {
-                    const uint16_t* vp_mine = st.beam_v + (live ? kvj[j] : 0) * D;
-                    __syncwarp();
-                    constexpr int kRowsPer = 32 / kChunks;  // rows one warp instruction covers
-                    constexpr int kIters = 32 / kRowsPer;
-                    uint4 vt[kIters];  // every load in flight before the first store
+            // ---- the beam part: the row's private keys, one at a time
+            constexpr int kKC = D / 8;                   // 16-byte chunks of a bf16 row
+            constexpr int kSlotBytes = 4 * D + 16;       // a key's K row, V row, one chunk of padding
+            constexpr int kArea = P::kKVTile / 2;        // each softmax warp's share of the two rings
+            constexpr int kSlots = kArea / kSlotBytes;   // keys staged at a time
+            uint8_t* area = smem + P::kKOff + (warp - 4) * kArea;
+            const int L = st.n_levels;
+            const int row_off = st.req[U.req].row_off;
+            auto key_row = [&](int j, int pool) -> int64_t {
+                return kScore ? ((int64_t)layer * st.rows + pool) * st.n_kv_heads + U.head
+                              : (((int64_t)layer * (L - 1) + j) * st.rows + pool) * st.n_kv_heads + U.head;
+            };
+            const uint4* qg = reinterpret_cast<const uint4*>(q + ri.orow_idx * D);
+            const uint8_t* qs = smem + P::kQOff + i * P::kQTile + row_t * 128;  // this row in the Q tile
+            // fold one key (its K and V rows) into (M, den, a)
+            auto fold = [&](const uint4* kp, const uint4* vp) {
+                float d0 = 0.f, d1 = 0.f;
+#pragma unroll 4
+                for (int c = 0; c < kKC; ++c) {
+                    const uint4 qa = staged ? *reinterpret_cast<const uint4*>(qs + (c >> 3) * P::kBoxBytes +
+                                                                              (((c & 7) ^ (row_t & 7)) << 4))
+                                            : __ldg(qg + c);
+                    const uint4 ka = kp[c];
+                    const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
 #pragma unroll
-                    for (int it = 0; it < kIters; ++it) {
-                        const int r = it * kRowsPer + lane / kChunks, c = lane % kChunks;
-                        const uint16_t* vp = reinterpret_cast<const uint16_t*>(
-                            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(vp_mine), r));
-                        vt[it] = __ldg(reinterpret_cast<const uint4*>(vp) + c);
-                    }
-#pragma unroll
-                    for (int it = 0; it < kIters; ++it) {
-                        const int r = it * kRowsPer + lane / kChunks, c = lane % kChunks;
-                        *reinterpret_cast<uint4*>(stg + (r * kChunks + (c ^ (r & (kChunks - 1)))) * 16) = vt[it];
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int c = 0; c < kChunks && live; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(
-                            stg + (lane * kChunks + (c ^ (lane & (kChunks - 1)))) * 16);
-                        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int h2 = 0; h2 < 4; ++h2) {
-                            a[8 * c + 2 * h2] = fmaf(w_j[j], __uint_as_float(vw[h2] << 16), a[8 * c + 2 * h2]);
-                            a[8 * c + 2 * h2 + 1] = fmaf(w_j[j], __uint_as_float(vw[h2] & 0xFFFF0000u), a[8 * c + 2 * h2 + 1]);
-                        }
-                    }
-                } else if (live) {
-                    const uint4* vp = reinterpret_cast<const uint4*>(st.beam_v + kvj[j] * D);
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-                        const uint4 v = __ldg(vp + c);
-                        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int h2 = 0; h2 < 4; ++h2) {
-                            a[8 * c + 2 * h2] = fmaf(w_j[j], __uint_as_float(vw[h2] << 16), a[8 * c + 2 * h2]);
-                            a[8 * c + 2 * h2 + 1] = fmaf(w_j[j], __uint_as_float(vw[h2] & 0xFFFF0000u), a[8 * c + 2 * h2 + 1]);
-                        }
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        d0 = fmaf(bf_lo(qw[h2]), bf_lo(kw[h2]), d0);
+                        d1 = fmaf(bf_hi(qw[h2]), bf_hi(kw[h2]), d1);
                     }
                 }
+                const float s = (d0 + d1) * scale;
+                if (s > M) {
+                    const float r = __expf(M - s);
+                    den *= r;
+#pragma unroll
+                    for (int c = 0; c < D; ++c) a[c] *= r;
+                    M = s;
+                }
+                const float pw = __expf(s - M);
+                den += pw;
+#pragma unroll
+                for (int c = 0; c < kKC; ++c) {
+                    const uint4 v = vp[c];
+                    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        a[8 * c + 2 * h2] = fmaf(pw, bf_lo(vw[h2]), a[8 * c + 2 * h2]);
+                        a[8 * c + 2 * h2 + 1] = fmaf(pw, bf_hi(vw[h2]), a[8 * c + 2 * h2 + 1]);
+                    }
+                }
+            };
+            if (staged) {
+                // the rings are free once the last key tile's S and PV MMAs have completed
+                const uint32_t kl = ktiles - 1;  // the CTA's last key tile
+                if (!(ok = wait_warp(bar(B_K_EMPTY + (kl & 1)), (kl >> 1) & 1, wt))) break;
+                if (!(ok = wait_warp(bar(B_V_EMPTY + (kl & 1)), (kl >> 1) & 1, wt))) break;
+                // Keys are numbered warp-wide and staged kSlots at a time.  Decode: key
+                // (level j, beam bl of the warp's beams) is j * nbw + bl.  Scoring: a key is a
+                // pool row, numbered from the warp's first one (its rows' segments are
+                // consecutive pool rows).
+                const int nbw = G >= 32 ? 1 : 32 / G;        // beams the warp's rows belong to
+                const int bl = G >= 32 ? 0 : lane / G;       // this row's beam among them
+                const int b_first = U.beam0 + i * (kTileRows / G) + (quarter * 32) / G;
+                int lo = 0, total;
+                if constexpr (kScore) {
+                    lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(ri.live ? ri.pool0 : 0x7fffffff));
+                    const int hi = __reduce_max_sync(0xffffffffu, ri.live ? ri.pool0 + ri.n_priv - 1 : -1);
+                    total = hi >= lo ? hi - lo + 1 : 0;
+                } else {
+                    total = __reduce_max_sync(0xffffffffu, ri.n_priv) * nbw;
+                }
+                const int t = kScore ? 0 : st.req_step[U.req];
+                const int nb = kScore ? 0 : st.n_beams[U.req * (L + 1) + t];
+                const uint32_t bbar = bar(B_BEAM + warp - 4);
+                const uint32_t area_s = smem_u32(area);
+#pragma unroll 1
+                for (int p0 = 0; p0 < total && ok; p0 += kSlots) {
+                    // copies: lane l stages key p0 + l
+                    const int idx = p0 + lane;
+                    int64_t key = -1;
+                    if (lane < kSlots && idx < total) {
+                        if constexpr (kScore) {
+                            key = key_row(0, lo + idx);
+                        } else {
+                            const int j = idx / nbw, b = b_first + (idx - j * nbw);
+                            if (b < st.req[U.req].width && b < nb)
+                                key = key_row(j, row_off + __ldg(st.path + ((int64_t)(t - 1) * st.rows + row_off + b) * L + j));
+                        }
+                    }
+                    const unsigned copies = __ballot_sync(0xffffffffu, key >= 0);
+                    if (lane == 0) mbar_expect_tx(bbar, (uint32_t)__popc(copies) * (uint32_t)(4 * D));
+                    __syncwarp();
+                    if (key >= 0) {
+                        bulk_load(area_s + lane * kSlotBytes, st.beam_k + key * D, 2 * D, bbar);
+                        bulk_load(area_s + lane * kSlotBytes + 2 * D, st.beam_v + key * D, 2 * D, bbar);
+                    }
+                    const uint32_t par = bcnt & 1;
+                    ++bcnt;
+                    if (!(ok = wait_warp(bbar, par, wt))) {
+                        wait_drain(bbar, par);  // no copy may land after the CTA has gone
+                        break;
+                    }
+                    for (int j = 0; j < ri.n_priv; ++j) {
+                        const int kidx = kScore ? ri.pool0 + j - lo : j * nbw + bl;
+                        if (kidx < p0 || kidx >= p0 + kSlots) continue;
+                        const uint8_t* sl = area + (kidx - p0) * kSlotBytes;
+                        fold(reinterpret_cast<const uint4*>(sl), reinterpret_cast<const uint4*>(sl + 2 * D));
+                    }
+                    __syncwarp();  // every row is done with these slots before they are refilled
+                }
+                if (!ok) break;
+            } else {
+                for (int j = 0; j < ri.n_priv; ++j) {
+                    const int pool = kScore ? ri.pool0 + j : row_off + __ldg(ri.path + j);
+                    const int64_t key = key_row(j, pool);
+                    fold(reinterpret_cast<const uint4*>(st.beam_k + key * D), reinterpret_cast<const uint4*>(st.beam_v + key * D));
+                }
+            }
+            {
+                // dead beams come out as exact zeros: none of their (unwritten) inputs is used
+                const float inv_den = ri.live ? 1.f / den : 0.f;
+#pragma unroll
+                for (int c = 0; c < D; ++c) a[c] = ri.live ? a[c] * inv_den : 0.f;
             }
             // ---- bf16 output rows (rows beyond the request are another request's: not written)
+            constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per bf16 row
             if (staged) {
-                __syncwarp();
+                uint8_t* stg = area;  // the warp's own share of the rings, free again
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
                     *reinterpret_cast<uint4*>(stg + (lane * kChunks + (c ^ (lane & (kChunks - 1)))) * 16) =
                         make_uint4(pack_bf16x2(a[8 * c], a[8 * c + 1]), pack_bf16x2(a[8 * c + 2], a[8 * c + 3]),
                                    pack_bf16x2(a[8 * c + 4], a[8 * c + 5]), pack_bf16x2(a[8 * c + 6], a[8 * c + 7]));
                 __syncwarp();
-                uint16_t* op_mine = out + orow_idx * D;
-                constexpr int kRowsPer = 32 / kChunks;
+                constexpr int kRowsPer = 32 / kChunks;  // rows one warp instruction covers
+                const int c = lane % kChunks;
+#pragma unroll 1
                 for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
-                    const int r = r0 + lane / kChunks, c = lane % kChunks;
-                    uint16_t* op = reinterpret_cast<uint16_t*>(
-                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(op_mine), r));
-                    const int ok_r = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, r);
+                    const int r = r0 + lane / kChunks;
+                    const long long orow = __shfl_sync(0xffffffffu, (long long)ri.orow_idx, r);
+                    const int ok_r = __shfl_sync(0xffffffffu, ri.row_ok ? 1 : 0, r);
                     if (ok_r)
-                        reinterpret_cast<uint4*>(op)[c] =
+                        reinterpret_cast<uint4*>(out + orow * D)[c] =
                             *reinterpret_cast<const uint4*>(stg + (r * kChunks + (c ^ (r & (kChunks - 1)))) * 16);
                 }
-            } else if (row_ok) {
-                uint4* dst = reinterpret_cast<uint4*>(out + orow_idx * D);
+            } else if (ri.row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(out + ri.orow_idx * D);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
                     dst[c] = make_uint4(pack_bf16x2(a[8 * c], a[8 * c + 1]), pack_bf16x2(a[8 * c + 2], a[8 * c + 3]),
                                         pack_bf16x2(a[8 * c + 4], a[8 * c + 5]), pack_bf16x2(a[8 * c + 6], a[8 * c + 7]));
             }
+        }
+        if (pend_flag != nullptr) {
+            __threadfence();
+            *reinterpret_cast<volatile uint32_t*>(pend_flag) = 1u;
         }
     }
     tc_fence_before();
@@ -965,11 +1006,10 @@ cudaError_t launch_attn(const GrState& st, const CUtensorMap& qmap, int layer, c
                         int64_t wait_limit_ns, cudaStream_t s) {
     const float scale = 1.f / sqrtf((float)st.head_dim);
     const float scale_log2 = scale * 1.4426950408889634f;
+    if (st.head_dim != 128 && st.head_dim != 64) return cudaErrorInvalidValue;
     if (st.head_dim == 128)
         return launch_ctx_attn_d<128, kScore>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
-    if (st.head_dim == 64)
-        return launch_ctx_attn_d<64, kScore>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
-    return cudaErrorInvalidValue;
+    return launch_ctx_attn_d<64, kScore>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
 }
 
 cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
