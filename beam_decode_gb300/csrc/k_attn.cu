@@ -101,6 +101,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// a store whose line L2 should keep (evict_last policy): a published piece waits there
+// for its merger
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void st_keep(float4* p, float4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w), "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void tmap_acquire(const void* tmap) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmap) : "memory");
 }
@@ -701,11 +713,84 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 ++tiles;
             }
             if (!ok) break;
+            const float lse_own = m_used * scale + logf(l);
+            const float inv_l = 1.f / l;
+            // A merging job reads its pieces' ready flags and log-sum-exps while its last PV
+            // MMAs are still running: the weights of the parts are known when O arrives.
+            constexpr int kPieceRegs = 4;
+            const int n_other = merger ? U.n_slots - 1 : 0;
+            const float* lse_col = st.lse_part + (int64_t)U.first_slot * kUnitRows + prow;
+            float wp[kPieceRegs];
+            float M = lse_own, w_own = 1.f, den = 1.f;
+            if (merger) {
+                bool have = true;
+                if (ri.live)
+                    for (int pp = 1; pp <= n_other && have; ++pp)
+                        have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, 1u, wt);
+                if (__any_sync(0xffffffffu, !have)) { ok = false; break; }
+                __threadfence();
+                // the context part: own O and the published pieces, relative to the max M of
+                // their log-sum-exps; a and den stay unnormalised until the end
+#pragma unroll
+                for (int pp = 0; pp < kPieceRegs; ++pp)
+                    wp[pp] = (ri.live && pp < n_other) ? __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) : -CUDART_INF_F;
+#pragma unroll
+                for (int pp = 0; pp < kPieceRegs; ++pp) M = fmaxf(M, wp[pp]);
+                for (int pp = kPieceRegs + 1; ri.live && pp <= n_other; ++pp)
+                    M = fmaxf(M, __ldcg(lse_col + (int64_t)pp * kUnitRows));
+                w_own = __expf(lse_own - M);
+                den = w_own;
+#pragma unroll
+                for (int pp = 0; pp < kPieceRegs; ++pp) {
+                    wp[pp] = pp < n_other ? __expf(wp[pp] - M) : 0.f;
+                    den += wp[pp];
+                }
+            }
+            // The staged merge (the CTA's last job) copies its rows' BeamKV keys into the
+            // freed rings.  Keys are numbered warp-wide and staged kSlots at a time.  Decode:
+            // key (level j, beam bl of the warp's beams) is j * nbw + bl.  Scoring: a key is a
+            // pool row, numbered from the warp's first one (its rows' segments are consecutive
+            // pool rows).  The first batch's ancestry lookups are done here, before O arrives.
+            constexpr int kSlotBytes = 4 * D + 16;       // a key's K row, V row, one chunk of padding
+            constexpr int kArea = P::kKVTile / 2;        // each softmax warp's share of the two rings
+            constexpr int kSlots = kArea / kSlotBytes;   // keys staged at a time
+            const bool staged = merger && jb == jr.y - 1;
+            const int L = st.n_levels;
+            const int row_off = st.req[U.req].row_off;
+            const int nbw = G >= 32 ? 1 : 32 / G;        // beams the warp's rows belong to
+            const int bl = G >= 32 ? 0 : lane / G;       // this row's beam among them
+            const int b_first = U.beam0 + i * (kTileRows / G) + (quarter * 32) / G;
+            auto key_row = [&](int j, int pool) -> int64_t {
+                return kScore ? ((int64_t)layer * st.rows + pool) * st.n_kv_heads + U.head
+                              : (((int64_t)layer * (L - 1) + j) * st.rows + pool) * st.n_kv_heads + U.head;
+            };
+            int lo = 0, total = 0;
+            auto key_of = [&](int p0) -> int64_t {  // the key lane l stages in batch p0 (-1: none)
+                const int idx = p0 + lane;
+                if (lane >= kSlots || idx >= total) return -1;
+                if constexpr (kScore) {
+                    return key_row(0, lo + idx);
+                } else {
+                    const int t = st.req_step[U.req];
+                    const int j = idx / nbw, b = b_first + (idx - j * nbw);
+                    if (b >= st.req[U.req].width || b >= st.n_beams[U.req * (L + 1) + t]) return -1;
+                    return key_row(j, row_off + __ldg(st.path + ((int64_t)(t - 1) * st.rows + row_off + b) * L + j));
+                }
+            };
+            int64_t key0 = -1;
+            if (staged) {
+                if constexpr (kScore) {
+                    lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(ri.live ? ri.pool0 : 0x7fffffff));
+                    const int hi = __reduce_max_sync(0xffffffffu, ri.live ? ri.pool0 + ri.n_priv - 1 : -1);
+                    total = hi >= lo ? hi - lo + 1 : 0;
+                } else {
+                    total = __reduce_max_sync(0xffffffffu, ri.n_priv) * nbw;
+                }
+                key0 = key_of(0);
+            }
             // epilogue
             if (!(ok = wait_warp(bar(B_O_FULL + i), jobs & 1, wt))) break;
             tc_fence_after();
-            const float lse_own = m_used * scale + logf(l);
-            const float inv_l = 1.f / l;
             uint32_t ov[D];  // this piece's unnormalised O row
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_base + P::o_col(i) + 32 * c, ov + 32 * c);
@@ -721,11 +806,13 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 // rows' 16-byte chunks of one column group per instruction (512 bytes).
                 if (ri.live) {
                     float4* dst = reinterpret_cast<float4*>(st.o_part) + (int64_t)J.slot * (D / 4) * kUnitRows + prow;
+                    const uint64_t keep = l2_evict_last();
 #pragma unroll
                     for (int c = 0; c < D / 4; ++c)
-                        __stcg(dst + (int64_t)c * kUnitRows,
-                               make_float4(__uint_as_float(ov[4 * c]) * inv_l, __uint_as_float(ov[4 * c + 1]) * inv_l,
-                                           __uint_as_float(ov[4 * c + 2]) * inv_l, __uint_as_float(ov[4 * c + 3]) * inv_l));
+                        st_keep(dst + (int64_t)c * kUnitRows,
+                                make_float4(__uint_as_float(ov[4 * c]) * inv_l, __uint_as_float(ov[4 * c + 1]) * inv_l,
+                                           __uint_as_float(ov[4 * c + 2]) * inv_l, __uint_as_float(ov[4 * c + 3]) * inv_l),
+                                keep);
                     __stcg(st.lse_part + (int64_t)J.slot * kUnitRows + prow, lse_own);
                     pend_flag = st.piece_flag + (int64_t)J.slot * kUnitRows + prow;
                 }
@@ -741,80 +828,15 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             // (bulk copies, 31 key slots at a time), reads q from the job's Q tile, and
             // finally passes its bf16 output rows through the same space to write them
             // coalesced.  Otherwise every row reads q, K and V from global memory.
-            const bool staged = (jb == jr.y - 1);
-            const int n_other = U.n_slots - 1;
-            bool have = true;
-            if (ri.live)
-                for (int pp = 1; pp <= n_other && have; ++pp)
-                    have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, 1u, wt);
-            if (__any_sync(0xffffffffu, !have)) { ok = false; break; }
-            __threadfence();
-            // ---- the context part: own O and the published pieces, relative to the max M of
-            // their log-sum-exps; a and den stay unnormalised until the end
-            constexpr int kPieceRegs = 4;
-            const float* lse_col = st.lse_part + (int64_t)U.first_slot * kUnitRows + prow;
-            float wp[kPieceRegs];
-#pragma unroll
-            for (int pp = 0; pp < kPieceRegs; ++pp)
-                wp[pp] = (ri.live && pp < n_other) ? __ldcg(lse_col + (int64_t)(pp + 1) * kUnitRows) : -CUDART_INF_F;
-            float M = lse_own;
-#pragma unroll
-            for (int pp = 0; pp < kPieceRegs; ++pp) M = fmaxf(M, wp[pp]);
-            for (int pp = kPieceRegs + 1; ri.live && pp <= n_other; ++pp)
-                M = fmaxf(M, __ldcg(lse_col + (int64_t)pp * kUnitRows));
-            const float w_own = __expf(lse_own - M);
-            float den = w_own;
-#pragma unroll
-            for (int pp = 0; pp < kPieceRegs; ++pp) {
-                wp[pp] = pp < n_other ? __expf(wp[pp] - M) : 0.f;
-                den += wp[pp];
-            }
             float* a = reinterpret_cast<float*>(ov);  // the row accumulates in place of O
             {
                 const float c_own = ri.live ? w_own * inv_l : 0.f;
 #pragma unroll
                 for (int c = 0; c < D; ++c) a[c] = ri.live ? __uint_as_float(ov[c]) * c_own : 0.f;
             }
-#pragma unroll 1
-            for (int pp = 1; ri.live && pp <= n_other; ++pp) {
-                float w = 0.f;
-#pragma unroll
-                for (int k = 0; k < kPieceRegs; ++k) w = (k == pp - 1) ? wp[k] : w;
-                if (pp > kPieceRegs) {
-                    w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
-                    den += w;
-                }
-                const float4* src =
-                    reinterpret_cast<const float4*>(st.o_part) + (int64_t)(U.first_slot + pp) * (D / 4) * kUnitRows + prow;
-                constexpr int kBatch = D / 16;  // chunks per batch of loads
-#pragma unroll
-                for (int c0 = 0; c0 < D / 4; c0 += kBatch) {
-                    float4 x[kBatch];
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) x[u] = __ldcg(src + (int64_t)(c0 + u) * kUnitRows);
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) {
-                        float* ac = a + 4 * (c0 + u);
-                        ac[0] = fmaf(w, x[u].x, ac[0]);
-                        ac[1] = fmaf(w, x[u].y, ac[1]);
-                        ac[2] = fmaf(w, x[u].z, ac[2]);
-                        ac[3] = fmaf(w, x[u].w, ac[3]);
-                    }
-                }
-                st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
-            }
-            // ---- the beam part: the row's private keys, one at a time
+            // ---- the beam part's set-up: the row's private keys are folded in one at a time
             constexpr int kKC = D / 8;                   // 16-byte chunks of a bf16 row
-            constexpr int kSlotBytes = 4 * D + 16;       // a key's K row, V row, one chunk of padding
-            constexpr int kArea = P::kKVTile / 2;        // each softmax warp's share of the two rings
-            constexpr int kSlots = kArea / kSlotBytes;   // keys staged at a time
             uint8_t* area = smem + P::kKOff + (warp - 4) * kArea;
-            const int L = st.n_levels;
-            const int row_off = st.req[U.req].row_off;
-            auto key_row = [&](int j, int pool) -> int64_t {
-                return kScore ? ((int64_t)layer * st.rows + pool) * st.n_kv_heads + U.head
-                              : (((int64_t)layer * (L - 1) + j) * st.rows + pool) * st.n_kv_heads + U.head;
-            };
             const uint4* qg = reinterpret_cast<const uint4*>(q + ri.orow_idx * D);
             const uint8_t* qs = smem + P::kQOff + i * P::kQTile + row_t * 128;  // this row in the Q tile
             // fold one key (its K and V rows) into (M, den, a)
@@ -854,51 +876,60 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                     }
                 }
             };
+            const uint32_t bbar = bar(B_BEAM + warp - 4);
+            const uint32_t area_s = smem_u32(area);
+            auto copy = [&](int64_t key) {  // lane l stages one key (or none: key < 0) in slot l
+                const unsigned copies = __ballot_sync(0xffffffffu, key >= 0);
+                if (lane == 0) mbar_expect_tx(bbar, (uint32_t)__popc(copies) * (uint32_t)(4 * D));
+                __syncwarp();
+                if (key >= 0) {
+                    bulk_load(area_s + lane * kSlotBytes, st.beam_k + key * D, 2 * D, bbar);
+                    bulk_load(area_s + lane * kSlotBytes + 2 * D, st.beam_v + key * D, 2 * D, bbar);
+                }
+            };
             if (staged) {
-                // the rings are free once the last key tile's S and PV MMAs have completed
+                // the rings are free once the last key tile's S and PV MMAs have completed;
+                // the first batch of copies goes out before the pieces are read, so that the
+                // two overlap
                 const uint32_t kl = ktiles - 1;  // the CTA's last key tile
                 if (!(ok = wait_warp(bar(B_K_EMPTY + (kl & 1)), (kl >> 1) & 1, wt))) break;
                 if (!(ok = wait_warp(bar(B_V_EMPTY + (kl & 1)), (kl >> 1) & 1, wt))) break;
-                // Keys are numbered warp-wide and staged kSlots at a time.  Decode: key
-                // (level j, beam bl of the warp's beams) is j * nbw + bl.  Scoring: a key is a
-                // pool row, numbered from the warp's first one (its rows' segments are
-                // consecutive pool rows).
-                const int nbw = G >= 32 ? 1 : 32 / G;        // beams the warp's rows belong to
-                const int bl = G >= 32 ? 0 : lane / G;       // this row's beam among them
-                const int b_first = U.beam0 + i * (kTileRows / G) + (quarter * 32) / G;
-                int lo = 0, total;
-                if constexpr (kScore) {
-                    lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(ri.live ? ri.pool0 : 0x7fffffff));
-                    const int hi = __reduce_max_sync(0xffffffffu, ri.live ? ri.pool0 + ri.n_priv - 1 : -1);
-                    total = hi >= lo ? hi - lo + 1 : 0;
-                } else {
-                    total = __reduce_max_sync(0xffffffffu, ri.n_priv) * nbw;
-                }
-                const int t = kScore ? 0 : st.req_step[U.req];
-                const int nb = kScore ? 0 : st.n_beams[U.req * (L + 1) + t];
-                const uint32_t bbar = bar(B_BEAM + warp - 4);
-                const uint32_t area_s = smem_u32(area);
+                if (total > 0) copy(key0);
+            }
+            // ---- the published pieces
 #pragma unroll 1
-                for (int p0 = 0; p0 < total && ok; p0 += kSlots) {
-                    // copies: lane l stages key p0 + l
-                    const int idx = p0 + lane;
-                    int64_t key = -1;
-                    if (lane < kSlots && idx < total) {
-                        if constexpr (kScore) {
-                            key = key_row(0, lo + idx);
-                        } else {
-                            const int j = idx / nbw, b = b_first + (idx - j * nbw);
-                            if (b < st.req[U.req].width && b < nb)
-                                key = key_row(j, row_off + __ldg(st.path + ((int64_t)(t - 1) * st.rows + row_off + b) * L + j));
-                        }
+            for (int pp = 1; ri.live && pp <= n_other; ++pp) {
+                float w = 0.f;
+#pragma unroll
+                for (int k = 0; k < kPieceRegs; ++k) w = (k == pp - 1) ? wp[k] : w;
+                if (pp > kPieceRegs) {
+                    w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
+                    den += w;
+                }
+                const float4* src =
+                    reinterpret_cast<const float4*>(st.o_part) + (int64_t)(U.first_slot + pp) * (D / 4) * kUnitRows + prow;
+                constexpr int kBatch = D / 8;  // chunks per batch of loads
+#pragma unroll
+                for (int c0 = 0; c0 < D / 4; c0 += kBatch) {
+                    float4 x[kBatch];
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) x[u] = __ldcg(src + (int64_t)(c0 + u) * kUnitRows);
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        float* ac = a + 4 * (c0 + u);
+                        ac[0] = fmaf(w, x[u].x, ac[0]);
+                        ac[1] = fmaf(w, x[u].y, ac[1]);
+                        ac[2] = fmaf(w, x[u].z, ac[2]);
+                        ac[3] = fmaf(w, x[u].w, ac[3]);
                     }
-                    const unsigned copies = __ballot_sync(0xffffffffu, key >= 0);
-                    if (lane == 0) mbar_expect_tx(bbar, (uint32_t)__popc(copies) * (uint32_t)(4 * D));
-                    __syncwarp();
-                    if (key >= 0) {
-                        bulk_load(area_s + lane * kSlotBytes, st.beam_k + key * D, 2 * D, bbar);
-                        bulk_load(area_s + lane * kSlotBytes + 2 * D, st.beam_v + key * D, 2 * D, bbar);
-                    }
+                }
+                st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
+            }
+            // ---- the beam part, one key at a time
+            if (staged) {
+#pragma unroll 1
+                for (int p0 = 0; p0 < total; p0 += kSlots) {
+                    if (p0 > 0) copy(key_of(p0));
                     const uint32_t par = bcnt & 1;
                     ++bcnt;
                     if (!(ok = wait_warp(bbar, par, wt))) {
