@@ -33,12 +33,13 @@
 // its first key range, which by construction of the schedule is the last job
 // of its CTA; the later ranges run at the start of the next CTAs and publish
 // their normalised fp32 piece, its log-sum-exp and a per-row ready flag,
-// which the merger clears once it has read the row.  The first range merges them with its own O
-// (still in registers) and with the beam part -- the t BeamKV keys found
-// through the beam's ancestry row (levels 0..t-1) -- by a log-sum-exp
-// combine, and writes the bf16 output row.  Rows of dead beams are written
-// as zeros.  The launch is cooperative, so every CTA a merger waits for is
-// resident.
+// which the merger clears once it has read the row.  The first range merges,
+// by a log-sum-exp combine, its own O (from TMEM), the pieces, and the beam
+// part -- the t BeamKV keys found through the beam's ancestry row (levels
+// 0..t-1), folded in one key at a time per row, from K/V rows bulk-copied into
+// the freed shared-memory rings -- and writes the bf16 output row.  Rows of
+// dead beams are written as zeros.  The launch is cooperative, so every CTA a
+// merger waits for is resident.
 
 // Every wait inside k_ctx_attn is bounded: past the limit the kernel flags
 // GR_ERR_TIMEOUT, drains the copies and MMAs it issued, frees TMEM and returns.
