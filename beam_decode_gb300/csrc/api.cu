@@ -348,38 +348,76 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     }
     int64_t tiles_all = 0;
     for (auto& u : s.units) tiles_all += u.n_tiles;
-    int n_cta = (int)std::min<int64_t>(std::max(n_sm, 1), tiles_all);
-    s.cta_jobs.resize(n_cta);
-    // walk units and tiles in order, cutting at cost boundaries
-    int cta = 0;
-    int64_t acc = 0;
-    int64_t bound = (total * (cta + 1) + n_cta - 1) / n_cta;
-    int job_begin = 0;
-    for (int ui = 0; ui < (int)s.units.size(); ++ui) {
-        GrAttnUnit& u = s.units[ui];
-        u.first_slot = (int)s.jobs.size();
-        int t0 = 0;
-        for (int t = 0; t < u.n_tiles; ++t) {
-            acc += u.nqt;
-            const bool last_tile = (t == u.n_tiles - 1);
-            const bool cut = acc >= bound && cta < n_cta - 1;
-            if (cut || last_tile) {
-                GrAttnJob j{ui, t0, t + 1, (int)s.jobs.size()};
-                s.jobs.push_back(j);
-                t0 = t + 1;
+    const int n_cta = (int)std::min<int64_t>(std::max(n_sm, 1), tiles_all);
+    // Cost model of a CTA's time (measured on the attention kernel at ctx 5000, in units of
+    // ~83 ns): a key tile costs 20 with two query tiles (they ping-pong) and 17 with one;
+    // every job after a CTA's first costs kSwitch more (publish, the next job's Q, pipeline
+    // refill); a unit's first key range, the merger, costs kMerge more (pieces, BeamKV keys,
+    // output).  The makespan bound T is the smallest for which a greedy walk fits every
+    // unit into n_cta CTAs: units and key tiles in order (so the units of a KV head stay on
+    // neighbouring CTAs), a unit cut where a CTA's budget runs out.  A cut unit's first range
+    // is then the last job of its CTA and its later ranges are the first jobs of the next
+    // CTAs, which publish them before they wait for anything.
+    constexpr int64_t kSwitch = 36, kMerge = 105;
+    auto tile_cost = [](const GrAttnUnit& u) -> int64_t { return u.nqt == 2 ? 20 : 17; };
+    // returns the CTAs used (n_cta + 1: does not fit); with emit, writes jobs and ranges
+    auto walk = [&](int64_t T, bool emit) -> int {
+        int cta = 0, njobs = 0, job_begin = 0;
+        int64_t load = 0;
+        if (emit) s.jobs.clear();
+        auto next_cta = [&]() {
+            if (emit && cta < n_cta) s.cta_jobs[cta] = make_int2(job_begin, (int)s.jobs.size());
+            job_begin = (int)s.jobs.size();
+            ++cta;
+            load = 0;
+            njobs = 0;
+        };
+        for (int ui = 0; ui < (int)s.units.size(); ++ui) {
+            GrAttnUnit& u = s.units[ui];
+            if (emit) u.first_slot = (int)s.jobs.size();
+            const int64_t tc = tile_cost(u);
+            int t0 = 0;
+            while (t0 < u.n_tiles) {
+                if (cta >= n_cta) return n_cta + 1;
+                const int64_t sw = njobs > 0 ? kSwitch : 0;
+                const int64_t merge = t0 == 0 ? kMerge : 0;
+                const int rem = u.n_tiles - t0;
+                int take = rem;
+                if (load + sw + merge + rem * tc > T) {
+                    const int64_t fit = (T - load - sw - merge) / tc;
+                    if (fit < 1) {
+                        if (njobs == 0) return n_cta + 1;  // not even one tile in an empty CTA
+                        next_cta();
+                        continue;
+                    }
+                    take = (int)std::min<int64_t>(fit, rem);
+                }
+                if (emit) s.jobs.push_back(GrAttnJob{ui, t0, t0 + take, (int)s.jobs.size()});
+                load += sw + merge + take * tc;
+                ++njobs;
+                t0 += take;
+                if (t0 < u.n_tiles) next_cta();  // the rest of the unit opens the next CTA
             }
-            if (cut) {
-                s.cta_jobs[cta] = make_int2(job_begin, (int)s.jobs.size());
-                job_begin = (int)s.jobs.size();
-                ++cta;
-                bound = (total * (cta + 1) + n_cta - 1) / n_cta;
-            }
+            if (emit) u.n_slots = (int)s.jobs.size() - u.first_slot;
         }
-        u.n_slots = (int)s.jobs.size() - u.first_slot;
+        const int used = cta + (njobs > 0 ? 1 : 0);
+        if (emit) {
+            next_cta();
+            for (int k = cta; k < n_cta; ++k) s.cta_jobs[k] = make_int2((int)s.jobs.size(), (int)s.jobs.size());
+        }
+        return used;
+    };
+    int64_t all = 0;
+    for (auto& u : s.units) all += kMerge + kSwitch + u.n_tiles * tile_cost(u);
+    int64_t lo = 1, hi = all;  // hi: one CTA takes everything, which always fits
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (walk(mid, false) <= n_cta) hi = mid;
+        else lo = mid + 1;
     }
-    s.cta_jobs[cta] = make_int2(job_begin, (int)s.jobs.size());
-    // CTAs that received no job (only possible when cuts ran ahead) get an empty range
-    for (int k = cta + 1; k < n_cta; ++k) s.cta_jobs[k] = make_int2((int)s.jobs.size(), (int)s.jobs.size());
+    s.cta_jobs.assign(n_cta, make_int2(0, 0));
+    walk(lo, true);
+    (void)total;
     return s;
 }
 
