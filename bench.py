@@ -484,7 +484,10 @@ def run_e2e(args, batch: DeviceBatch):
     """Same step through the public API with pinned host inputs copied in and the
     step's selection read back every step.  The copies run on their own stream,
     layer by layer, so that a layer's inputs arrive while earlier layers compute;
-    events keep every device buffer from being overwritten before its consumer ran."""
+    events keep every device buffer from being overwritten before its consumer ran.
+    The host issues the next step's copies before it reads the current step's
+    selection back, so the copy stream never waits for the read-back: each timed
+    step still holds one full set of input copies, one step and one read-back."""
     import torch
     w = batch.w
     beam = batch.beam
@@ -506,8 +509,7 @@ def run_e2e(args, batch: DeviceBatch):
     kv = [beam.kv_slot(l) for l in range(NL)]
     d2h = 0
 
-    def one():
-        nonlocal d2h
+    def copies():  # one step's inputs, host -> device
         with torch.cuda.stream(copy):
             for l in range(NL):
                 copy.wait_event(used[l])
@@ -518,6 +520,8 @@ def run_e2e(args, batch: DeviceBatch):
             copy.wait_event(used[NL])
             dx.copy_(host_x, non_blocking=True)
             arrived[NL].record(copy)
+
+    def step():
         beam.rewind(1)
         for l in range(NL):
             comp.wait_event(arrived[l])
@@ -527,19 +531,27 @@ def run_e2e(args, batch: DeviceBatch):
         beam.constrained_topk(dx)
         used[NL].record(comp)
         beam.advance()
+
+    def readback():
+        nonlocal d2h
         n = 0
-        for r in range(w.n_requests):  # the step's selection, read back (synchronises)
+        for r in range(w.n_requests):  # the step's selection, read back (synchronises the step)
             par, tok, nod, sc = beam.path(r, 1)
             n += (par.nbytes + tok.nbytes + sc.nbytes)
         d2h = n
 
+    copies()
     for _ in range(2):
-        one()
+        step()
+        copies()
+        readback()
     torch.cuda.synchronize()
     steps = max(3, args.steps // 4)
     t0 = time.perf_counter()
     for _ in range(steps):
-        one()
+        step()
+        copies()
+        readback()
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     # the host->device copy rate alone, for reading the number
