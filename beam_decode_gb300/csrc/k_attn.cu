@@ -114,6 +114,15 @@ __device__ __forceinline__ void st_keep(float4* p, float4 v, uint64_t pol) {
                  "f"(v.w), "l"(pol)
                  : "memory");
 }
+// untiled bulk copy shared -> global (bulk async-group completion)
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tmap_acquire(const void* tmap) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmap) : "memory");
 }
@@ -962,24 +971,18 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             // ---- bf16 output rows (rows beyond the request are another request's: not written)
             constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per bf16 row
             if (staged) {
-                uint8_t* stg = area;  // the warp's own share of the rings, free again
+                // each row through the warp's own share of the rings (free again; rows padded by
+                // one chunk against bank conflicts), then one bulk store per row
+                constexpr int kRowStride = 2 * D + 16;
+                uint8_t* stg = area + lane * kRowStride;
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    *reinterpret_cast<uint4*>(stg + (lane * kChunks + (c ^ (lane & (kChunks - 1)))) * 16) =
+                    *reinterpret_cast<uint4*>(stg + c * 16) =
                         make_uint4(pack_bf16x2(a[8 * c], a[8 * c + 1]), pack_bf16x2(a[8 * c + 2], a[8 * c + 3]),
                                    pack_bf16x2(a[8 * c + 4], a[8 * c + 5]), pack_bf16x2(a[8 * c + 6], a[8 * c + 7]));
-                __syncwarp();
-                constexpr int kRowsPer = 32 / kChunks;  // rows one warp instruction covers
-                const int c = lane % kChunks;
-#pragma unroll 1
-                for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
-                    const int r = r0 + lane / kChunks;
-                    const long long orow = __shfl_sync(0xffffffffu, (long long)ri.orow_idx, r);
-                    const int ok_r = __shfl_sync(0xffffffffu, ri.row_ok ? 1 : 0, r);
-                    if (ok_r)
-                        reinterpret_cast<uint4*>(out + orow * D)[c] =
-                            *reinterpret_cast<const uint4*>(stg + (r * kChunks + (c ^ (r & (kChunks - 1)))) * 16);
-                }
+                fence_proxy_async_smem();  // the row's generic writes, then the bulk copy reads them
+                if (ri.row_ok) bulk_store(out + ri.orow_idx * D, smem_u32(stg), 2 * D);
+                bulk_commit_and_wait_read();  // the shared rows have been read
             } else if (ri.row_ok) {
                 uint4* dst = reinterpret_cast<uint4*>(out + ri.orow_idx * D);
 #pragma unroll
