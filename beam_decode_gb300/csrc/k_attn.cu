@@ -898,12 +898,13 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 }
             };
             if (staged) {
-                // the rings are free once the last key tile's S and PV MMAs have completed;
-                // the first batch of copies goes out before the pieces are read, so that the
-                // two overlap
+                // Query tile 0's warps stage in the K ring, free once the last key tile's S
+                // MMAs (both tiles') have completed; tile 1's warps in the V ring, free once the
+                // last PV MMAs have (its own is done: O arrived).  No more tiles are loaded.
+                // The first batch of copies goes out before the pieces are read, so that the
+                // two overlap.
                 const uint32_t kl = ktiles - 1;  // the CTA's last key tile
-                if (!(ok = wait_warp(bar(B_K_EMPTY + (kl & 1)), (kl >> 1) & 1, wt))) break;
-                if (!(ok = wait_warp(bar(B_V_EMPTY + (kl & 1)), (kl >> 1) & 1, wt))) break;
+                if (!(ok = wait_warp(bar((i == 0 ? B_K_EMPTY : B_V_EMPTY) + (kl & 1)), (kl >> 1) & 1, wt))) break;
                 if (total > 0) copy(key0);
             }
             // ---- the published pieces
