@@ -421,6 +421,18 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     return s;
 }
 
+// Each unit gets its request's fixed fields, and each job a copy of its unit: starting a
+// job on the device then takes one table read.
+void finalize_jobs(Schedule& s, const GrReqDev* rq) {
+    for (auto& u : s.units) {
+        u.row_off = rq[u.req].row_off;
+        u.width = rq[u.req].width;
+        u.ctx_len = rq[u.req].ctx_len;
+        u.n_levels = rq[u.req].n_levels;
+    }
+    for (auto& j : s.jobs) j.u = s.units[j.unit];
+}
+
 WsLayout ws_layout(const gr_config* c, int n, int rows, const Caps& k) {
     WsLayout w{};
     size_t o = 0;
@@ -604,6 +616,7 @@ gr_status build_tables(gr_beam* h) {
                               s2, 64, kTileKeys, 1)) != GR_OK)
             return s;
     }
+    finalize_jobs(h->sched, rq);
     memcpy(img + w.jobs, h->sched.jobs.data(), sizeof(GrAttnJob) * h->sched.jobs.size());
     memcpy(img + w.cta_jobs, h->sched.cta_jobs.data(), sizeof(int2) * h->sched.cta_jobs.size());
     memcpy(img + w.units, h->sched.units.data(), sizeof(GrAttnUnit) * h->sched.units.size());
@@ -1274,6 +1287,7 @@ extern "C" gr_status gr_score_create(const gr_score_config* cfg, const gr_score_
                 return s;
             }
         }
+        finalize_jobs(sc, rq);
         memcpy(img.data() + w.jobs, sc.jobs.data(), sizeof(GrAttnJob) * sc.jobs.size());
         memcpy(img.data() + w.cta_jobs, sc.cta_jobs.data(), sizeof(int2) * sc.cta_jobs.size());
         memcpy(img.data() + w.units, sc.units.data(), sizeof(GrAttnUnit) * sc.units.size());

@@ -45,13 +45,6 @@ struct GrReqDev {
     const int64_t* leaf_item;  // [n_items]
 };
 
-// One piece of attention work: key tiles [t0, t1) of one unit.
-struct GrAttnJob {
-    int unit;
-    int t0, t1;
-    int slot;           // partial-result slot (== job index)
-};
-
 // A unit: up to two 128-row query tiles of one (request, KV head).
 struct GrAttnUnit {
     int req;
@@ -61,7 +54,21 @@ struct GrAttnUnit {
     int first_slot;     // jobs of the unit are slots [first_slot, first_slot + n_slots)
     int n_slots;
     int n_tiles;        // ceil(T_r / kTileKeys)
+    // the request's fixed fields, so that a job needs no request lookup
+    int row_off;        // first row of the request
+    int width;          // W_r
+    int ctx_len;        // T_r
+    int n_levels;       // L_r
     int pad;
+};
+
+// One piece of attention work: key tiles [t0, t1) of one unit.  It carries a copy of its
+// unit, so that starting a job takes one table read.
+struct GrAttnJob {
+    int unit;
+    int t0, t1;
+    int slot;           // partial-result slot (== job index)
+    GrAttnUnit u;
 };
 
 struct GrState {

@@ -343,7 +343,7 @@ template <bool kScore>
 __device__ __forceinline__ bool decoding(const GrState& st, const GrAttnUnit& U) {
     if constexpr (kScore) return true;  // multi-item scoring: one pass, every unit takes part
     const int t = st.req_step[U.req];
-    return t >= 1 && t < st.req[U.req].n_levels;
+    return t >= 1 && t < U.n_levels;
 }
 
 // ---------------------------------------------------------------------------
@@ -362,24 +362,23 @@ struct RowInfo {
 template <bool kScore>
 __device__ __forceinline__ RowInfo row_info(const GrState& st, const GrAttnUnit& U, int i, int row_t, int G) {
     RowInfo ri;
-    const GrReqDev& R = st.req[U.req];
     const int t = kScore ? 0 : st.req_step[U.req];
     ri.b = U.beam0 + i * (kTileRows / G) + row_t / G;
     const int g = row_t % G;
-    ri.row_ok = ri.b < R.width;
+    ri.row_ok = ri.b < U.width;
     ri.live = ri.row_ok && (kScore || ri.b < st.n_beams[U.req * (st.n_levels + 1) + t]);
-    ri.orow_idx = (int64_t)(R.row_off + ri.b) * st.n_q_heads + U.head * G + g;
+    ri.orow_idx = (int64_t)(U.row_off + ri.b) * st.n_q_heads + U.head * G + g;
     ri.pool0 = 0;
     ri.path = nullptr;
     ri.n_priv = 0;
     if constexpr (kScore) {
         if (ri.live) {
-            ri.n_priv = st.seg_pos[R.row_off + ri.b] + 1;
-            ri.pool0 = st.seg_first[R.row_off + ri.b];
+            ri.n_priv = st.seg_pos[U.row_off + ri.b] + 1;
+            ri.pool0 = st.seg_first[U.row_off + ri.b];
         }
     } else {
         ri.n_priv = ri.live ? t : 0;
-        ri.path = st.path + ((int64_t)(t - 1) * st.rows + R.row_off + ri.b) * st.n_levels;
+        ri.path = st.path + ((int64_t)(t - 1) * st.rows + U.row_off + ri.b) * st.n_levels;
     }
     return ri;
 }
@@ -479,8 +478,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             bool ok = true;
             for (int jb = jr.x; jb < jr.y && ok; ++jb) {
                 const GrAttnJob J = st.jobs[jb];
-                const GrAttnUnit U = st.units[J.unit];
-                const GrReqDev& R = st.req[U.req];
+                const GrAttnUnit& U = J.u;
                 if (!decoding<kScore>(st, U)) continue;
                 const CUtensorMap* km = st.tmaps + 2 * U.req;
                 const CUtensorMap* vm = km + 1;
@@ -493,7 +491,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 for (int i = 0; i < U.nqt; ++i)
                     for (int kb = 0; kb < P::kBoxes; ++kb)
                         tma_load_3d(sb + P::kQOff + i * P::kQTile + kb * P::kBoxBytes, &qmap, bar(B_Q_FULL), kb * 64,
-                                    U.head * G, R.row_off + U.beam0 + i * (kTileRows / G));
+                                    U.head * G, U.row_off + U.beam0 + i * (kTileRows / G));
                 ++p_qcnt;
                 const int z = layer * st.n_kv_heads + U.head;
                 for (int j = J.t0; j < J.t1; ++j) {
@@ -528,7 +526,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 uint32_t kit = 0, qcnt = 0, s_i[2] = {0, 0};
                 for (int jb = jr.x; jb < jr.y && ok; ++jb) {
                     const GrAttnJob J = st.jobs[jb];
-                    const GrAttnUnit U = st.units[J.unit];
+                    const GrAttnUnit& U = J.u;
                     if (!decoding<kScore>(st, U)) continue;
                     const int nqt = U.nqt;
                     const int n = J.t1 - J.t0;
@@ -563,7 +561,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 uint32_t vit = 0, pv_i[2] = {0, 0}, jobs_i[2] = {0, 0};
                 for (int jb = jr.x; jb < jr.y && ok; ++jb) {
                     const GrAttnJob J = st.jobs[jb];
-                    const GrAttnUnit U = st.units[J.unit];
+                    const GrAttnUnit& U = J.u;
                     if (!decoding<kScore>(st, U)) continue;
                     const int nqt = U.nqt;
                     const int n = J.t1 - J.t0;
@@ -639,13 +637,13 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
         uint32_t* pend_flag = nullptr;
         for (int jb = jr.x; jb < jr.y && ok; ++jb) {
             const GrAttnJob J = st.jobs[jb];
-            const GrAttnUnit U = st.units[J.unit];
+            const GrAttnUnit& U = J.u;
             if (!decoding<kScore>(st, U)) continue;
             const int n = J.t1 - J.t0;
             ktiles += n;  // key tiles the S issuer has taken through the K ring so far
             if (i >= U.nqt) continue;
             const RowInfo ri = row_info<kScore>(st, U, i, row_t, G);
-            const int ctx_len = st.req[U.req].ctx_len;
+            const int ctx_len = U.ctx_len;
             const bool merger = (J.slot == U.first_slot);
             if (pend_flag != nullptr) {
                 // the previous job's piece: its stores have drained by now, so the fence is cheap
@@ -766,7 +764,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             constexpr int kSlots = kArea / kSlotBytes;   // keys staged at a time
             const bool staged = merger && jb == jr.y - 1;
             const int L = st.n_levels;
-            const int row_off = st.req[U.req].row_off;
+            const int row_off = U.row_off;
             const int nbw = G >= 32 ? 1 : 32 / G;        // beams the warp's rows belong to
             const int bl = G >= 32 ? 0 : lane / G;       // this row's beam among them
             const int b_first = U.beam0 + i * (kTileRows / G) + (quarter * 32) / G;
@@ -783,7 +781,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 } else {
                     const int t = st.req_step[U.req];
                     const int j = idx / nbw, b = b_first + (idx - j * nbw);
-                    if (b >= st.req[U.req].width || b >= st.n_beams[U.req * (L + 1) + t]) return -1;
+                    if (b >= U.width || b >= st.n_beams[U.req * (L + 1) + t]) return -1;
                     return key_row(j, row_off + __ldg(st.path + ((int64_t)(t - 1) * st.rows + row_off + b) * L + j));
                 }
             };
