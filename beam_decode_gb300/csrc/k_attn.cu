@@ -70,6 +70,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -401,7 +404,7 @@ struct Plan {
     static constexpr int kKOff = kQOff + 2 * kQTile;
     static constexpr int kVOff = kKOff + kStages * kKVTile;
     static constexpr int kBarOff = kVOff + kStages * kKVTile;
-    static constexpr int kBytes = kBarOff + 256 + 1024;  // barriers, TMEM address, abort flag, alignment
+    static constexpr int kBytes = kBarOff + 512 + 1024;  // barriers, TMEM address, abort flag, alignment
     // TMEM columns
     static constexpr int kTmemCols = 512;
     static __device__ __forceinline__ int s_col(int i) { return i * 128; }
@@ -413,7 +416,8 @@ enum Bar {
     B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = 4, B_V_FULL = 6, B_V_EMPTY = 8,
     B_S_FULL = 10, B_P_FULL = 12, B_O_FULL = 14, B_O_EMPTY = 16, B_DRAIN = 18, B_PVD = 20,
     B_BEAM = 22,  // one per softmax warp: its BeamKV rows copied into the freed rings
-    B_COUNT = 30
+    B_MERGED = 30,  // a merging job that is not the CTA's last has finished with the rings and Q
+    B_COUNT = 31
 };
 
 constexpr int kAttnThreads = 384;
@@ -452,6 +456,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             mbar_init(bar(B_PVD + k), 1);
         }
         for (int k = 0; k < 8; ++k) mbar_init(bar(B_BEAM + k), 1);
+        mbar_init(bar(B_MERGED), 8);  // one arrival per softmax warp (see the merge's end)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -472,7 +477,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
     if (warp < 4) {
         regs_dec<56>();
         // producer state (kept for the drain)
-        uint32_t p_kit = 0, p_vit = 0, p_qcnt = 0;
+        uint32_t p_kit = 0, p_vit = 0, p_qcnt = 0, p_mcnt = 0;
     if (warp == 0) {
         if (lane == 0) {
             bool ok = true;
@@ -509,6 +514,12 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                         tma_load_3d(sb + P::kVOff + s * P::kKVTile + kb * P::kBoxBytes, vm, bar(B_V_FULL + s),
                                     kb * 64, j * kTileKeys, z);
                     ++p_vit;
+                }
+                // A merging job stages its BeamKV keys in the rings and reads q from its Q tile:
+                // the next job's loads wait until its merge is done.
+                if (ok && J.slot == U.first_slot && jb < jr.y - 1) {
+                    if (!(ok = wait1(bar(B_MERGED), p_mcnt & 1, wt))) break;
+                    ++p_mcnt;
                 }
             }
         }
@@ -754,15 +765,15 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                     den += wp[pp];
                 }
             }
-            // The staged merge (the CTA's last job) copies its rows' BeamKV keys into the
-            // freed rings.  Keys are numbered warp-wide and staged kSlots at a time.  Decode:
+            // The merge copies its rows' BeamKV keys into the freed rings (the producer holds
+            // the next job's loads until the merge is done).  Keys are numbered warp-wide and
+            // staged kSlots at a time.  Decode:
             // key (level j, beam bl of the warp's beams) is j * nbw + bl.  Scoring: a key is a
             // pool row, numbered from the warp's first one (its rows' segments are consecutive
             // pool rows).  The first batch's ancestry lookups are done here, before O arrives.
             constexpr int kSlotBytes = 4 * D + 16;       // a key's K row, V row, one chunk of padding
             constexpr int kArea = P::kKVTile / 2;        // each softmax warp's share of the two rings
             constexpr int kSlots = kArea / kSlotBytes;   // keys staged at a time
-            const bool staged = merger && jb == jr.y - 1;
             const int L = st.n_levels;
             const int row_off = U.row_off;
             const int nbw = G >= 32 ? 1 : 32 / G;        // beams the warp's rows belong to
@@ -786,7 +797,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 }
             };
             int64_t key0 = -1;
-            if (staged) {
+            if (merger) {
                 if constexpr (kScore) {
                     lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(ri.live ? ri.pool0 : 0x7fffffff));
                     const int hi = __reduce_max_sync(0xffffffffu, ri.live ? ri.pool0 + ri.n_priv - 1 : -1);
@@ -830,12 +841,12 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             // the other pieces (finished earlier, at the start of their CTAs' ranges) and the
             // beam part -- the row's private keys (decode: the t BeamKV tokens on its beam's
             // ancestry path; scoring: its own candidate up to itself), folded in one key at a
-            // time with an online max.  Each thread works on its own row.  When this is the
-            // CTA's last job, the K and V rings are free once the last key tile's MMAs have
-            // completed: each warp copies the private keys' K and V rows of its 32 rows there
-            // (bulk copies, 31 key slots at a time), reads q from the job's Q tile, and
-            // finally passes its bf16 output rows through the same space to write them
-            // coalesced.  Otherwise every row reads q, K and V from global memory.
+            // time with an online max.  Each thread works on its own row.  The K and V rings are
+            // free once the job's last key tile's MMAs have completed (the producer holds the
+            // next job's loads until this merge is done): each warp copies the private keys' K
+            // and V rows of its 32 rows there (bulk copies, 31 key slots at a time), reads q
+            // from the job's Q tile, and finally passes its bf16 output rows through the same
+            // space, one bulk store per row.
             float* a = reinterpret_cast<float*>(ov);  // the row accumulates in place of O
             {
                 const float c_own = ri.live ? w_own * inv_l : 0.f;
@@ -845,16 +856,14 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             // ---- the beam part's set-up: the row's private keys are folded in one at a time
             constexpr int kKC = D / 8;                   // 16-byte chunks of a bf16 row
             uint8_t* area = smem + P::kKOff + (warp - 4) * kArea;
-            const uint4* qg = reinterpret_cast<const uint4*>(q + ri.orow_idx * D);
             const uint8_t* qs = smem + P::kQOff + i * P::kQTile + row_t * 128;  // this row in the Q tile
             // fold one key (its K and V rows) into (M, den, a)
             auto fold = [&](const uint4* kp, const uint4* vp) {
                 float d0 = 0.f, d1 = 0.f;
 #pragma unroll 4
                 for (int c = 0; c < kKC; ++c) {
-                    const uint4 qa = staged ? *reinterpret_cast<const uint4*>(qs + (c >> 3) * P::kBoxBytes +
-                                                                              (((c & 7) ^ (row_t & 7)) << 4))
-                                            : __ldg(qg + c);
+                    const uint4 qa = *reinterpret_cast<const uint4*>(qs + (c >> 3) * P::kBoxBytes +
+                                                                     (((c & 7) ^ (row_t & 7)) << 4));
                     const uint4 ka = kp[c];
                     const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
 #pragma unroll
@@ -895,7 +904,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                     bulk_load(area_s + lane * kSlotBytes + 2 * D, st.beam_v + key * D, 2 * D, bbar);
                 }
             };
-            if (staged) {
+            {
                 // Query tile 0's warps stage in the K ring, free once the last key tile's S
                 // MMAs (both tiles') have completed; tile 1's warps in the V ring, free once the
                 // last PV MMAs have (its own is done: O arrived).  No more tiles are loaded.
@@ -935,7 +944,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
             }
             // ---- the beam part, one key at a time
-            if (staged) {
+            {
 #pragma unroll 1
                 for (int p0 = 0; p0 < total; p0 += kSlots) {
                     if (p0 > 0) copy(key_of(p0));
@@ -954,12 +963,6 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                     __syncwarp();  // every row is done with these slots before they are refilled
                 }
                 if (!ok) break;
-            } else {
-                for (int j = 0; j < ri.n_priv; ++j) {
-                    const int pool = kScore ? ri.pool0 + j : row_off + __ldg(ri.path + j);
-                    const int64_t key = key_row(j, pool);
-                    fold(reinterpret_cast<const uint4*>(st.beam_k + key * D), reinterpret_cast<const uint4*>(st.beam_v + key * D));
-                }
             }
             {
                 // dead beams come out as exact zeros: none of their (unwritten) inputs is used
@@ -969,7 +972,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             }
             // ---- bf16 output rows (rows beyond the request are another request's: not written)
             constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per bf16 row
-            if (staged) {
+            {
                 // each row through the warp's own share of the rings (free again; rows padded by
                 // one chunk against bank conflicts), then one bulk store per row
                 constexpr int kRowStride = 2 * D + 16;
@@ -982,13 +985,13 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 fence_proxy_async_smem();  // the row's generic writes, then the bulk copy reads them
                 if (ri.row_ok) bulk_store(out + ri.orow_idx * D, smem_u32(stg), 2 * D);
                 bulk_commit_and_wait_read();  // the shared rows have been read
-            } else if (ri.row_ok) {
-                uint4* dst = reinterpret_cast<uint4*>(out + ri.orow_idx * D);
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    dst[c] = make_uint4(pack_bf16x2(a[8 * c], a[8 * c + 1]), pack_bf16x2(a[8 * c + 2], a[8 * c + 3]),
-                                        pack_bf16x2(a[8 * c + 4], a[8 * c + 5]), pack_bf16x2(a[8 * c + 6], a[8 * c + 7]));
             }
+            // The producer may refill the rings and the Q tile.  Each merging warp arrives once
+            // its rows are done; with one query tile the first warpgroup's warps arrive for the
+            // second as well (a warpgroup without rows must not arrive on its own: it would run
+            // ahead to the next job's phase).
+            __syncwarp();
+            if (lane == 0 && jb < jr.y - 1) mbar_arrive_n(bar(B_MERGED), U.nqt == 1 ? 2u : 1u);
         }
         if (pend_flag != nullptr) {
             __threadfence();

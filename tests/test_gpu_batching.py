@@ -56,6 +56,21 @@ def test_finished_slot_takes_new_request():
     assert d.beam.status() == 0 and d2.beam.status() == 0
 
 
+def test_many_narrow_requests_share_ctas():
+    # 200 narrow requests (one query tile per unit, 1-4 key tiles) give far more units than
+    # CTAs: the schedule packs several whole units into a CTA, so merging jobs follow one
+    # another inside a CTA, each staging its BeamKV keys in the rings before the next loads
+    widths = [8, 16, 32, 64]
+    occ = [Occupant(ctx_len=90 + (37 * r) % 320, width=widths[r % 4], n_levels=2, n_items=60, key=100 + r)
+           for r in range(200)]
+    d = MixedDriver(occ, [o.width for o in occ], n_levels_max=2, seed=57)
+    for k in range(2):
+        r = d.step()
+        assert r["worst"] <= 1.0 and not r["mismatch"], (k, r["worst"], r["mismatch"][:3])
+    assert sorted(d.finished) == list(range(200))
+    assert d.beam.status() == 0
+
+
 def _batch(seed, device="cuda"):
     import torch
     L, NL, Hq, Hkv, D, V, C = 3, 2, 4, 2, 128, 4096, 64
