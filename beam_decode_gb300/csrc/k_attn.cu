@@ -642,26 +642,31 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         uint32_t tiles = 0, jobs = 0, ktiles = 0, bcnt = 0;
         bool ok = true;
-        // A published piece's ready flag is raised when the next job starts (or at the end),
-        // after that job's row set-up: by then its stores have drained and the release fence
-        // costs little.
+        // A published piece's ready flag is raised once the next job's first key tile is done
+        // (or when a job skips this warpgroup, or at the end): by then the piece's stores have
+        // drained and the release fence costs little.  Its merger reads it only at the end of
+        // its own job.
         uint32_t* pend_flag = nullptr;
+        auto raise_flag = [&]() {
+            if (pend_flag != nullptr) {
+                __threadfence();
+                *reinterpret_cast<volatile uint32_t*>(pend_flag) = 1u;
+                pend_flag = nullptr;
+            }
+        };
         for (int jb = jr.x; jb < jr.y && ok; ++jb) {
             const GrAttnJob J = st.jobs[jb];
             const GrAttnUnit& U = J.u;
             if (!decoding<kScore>(st, U)) continue;
             const int n = J.t1 - J.t0;
             ktiles += n;  // key tiles the S issuer has taken through the K ring so far
-            if (i >= U.nqt) continue;
+            if (i >= U.nqt) {
+                raise_flag();
+                continue;
+            }
             const RowInfo ri = row_info<kScore>(st, U, i, row_t, G);
             const int ctx_len = U.ctx_len;
             const bool merger = (J.slot == U.first_slot);
-            if (pend_flag != nullptr) {
-                // the previous job's piece: its stores have drained by now, so the fence is cheap
-                __threadfence();
-                *reinterpret_cast<volatile uint32_t*>(pend_flag) = 1u;
-                pend_flag = nullptr;
-            }
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int jj = 0; jj < n; ++jj) {
                 if (!(ok = wait_warp(bar(B_S_FULL + i), tiles & 1, wt))) break;
@@ -730,6 +735,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 tc_fence_before();
                 mbar_arrive(bar(B_P_FULL + i));
                 ++tiles;
+                raise_flag();
             }
             if (!ok) break;
             const float lse_own = m_used * scale + logf(l);
@@ -993,10 +999,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             __syncwarp();
             if (lane == 0 && jb < jr.y - 1) mbar_arrive_n(bar(B_MERGED), U.nqt == 1 ? 2u : 1u);
         }
-        if (pend_flag != nullptr) {
-            __threadfence();
-            *reinterpret_cast<volatile uint32_t*>(pend_flag) = 1u;
-        }
+        raise_flag();
     }
     tc_fence_before();
     named_bar_sync(1);
