@@ -248,6 +248,54 @@ def oracle_step_seconds(w: wl.Workload, budget_s: float = 12.0):
     return per_step, sample
 
 
+def batched_cpu_step_seconds(w: wl.Workload):
+    """Seconds per decode step of a batched fp32 CPU implementation on every host core (a
+    fairer CPU comparison than the naive oracle; reported beside it, never a parity check):
+    one (request, layer) slice of the shared-context attention as GQA matmuls
+    (all beams x query heads of a KV head against the request's context), scaled by the
+    layers and requests, plus the full-vocab log-softmax, candidate gather and per-request
+    top-K of one request's rows, scaled by the requests."""
+    import torch
+    threads = os.cpu_count() or 1
+    old = torch.get_num_threads()
+    torch.set_num_threads(threads)
+    try:
+        g = torch.Generator().manual_seed(w.seed * 1000 + 17)
+        W, T, D, G = w.beam_widths[0], w.ctx_lens[0], w.head_dim, w.n_q_heads // w.n_kv_heads
+        q = torch.randn(w.n_kv_heads, W * G, D, generator=g)
+        k = torch.randn(w.n_kv_heads, T, D, generator=g)
+        v = torch.randn(w.n_kv_heads, T, D, generator=g)
+        x = torch.randn(W, w.vocab, generator=g) * w.logit_std
+        score = torch.zeros(W)
+        scale = 1.0 / D ** 0.5
+
+        def attn():
+            s = torch.matmul(q, k.transpose(1, 2)) * scale
+            return torch.bmm(torch.softmax(s, dim=-1), v)
+
+        def select():
+            lp = torch.log_softmax(x, dim=-1)[:, w.code_base + w.codes_per_level:w.code_base + 2 * w.codes_per_level]
+            return torch.topk((score[:, None] + lp).reshape(-1), W)
+
+        attn(); select()  # warm the thread pool and allocator
+        reps = 3
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            attn()
+        att_s = (time.perf_counter() - t0) / reps
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            select()
+        sel_s = (time.perf_counter() - t0) / reps
+    finally:
+        torch.set_num_threads(old)
+    per_step = (att_s * w.n_layers + sel_s) * w.n_requests
+    sample = (f"torch CPU fp32 on {threads} threads: attention of one (request, layer) slice "
+              f"({att_s * 1e3:.1f} ms) x{w.n_layers} layers x{w.n_requests} requests; log-softmax + top-K of "
+              f"{W} rows ({sel_s * 1e3:.1f} ms) x{w.n_requests} requests")
+    return per_step, threads, sample
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -392,6 +440,11 @@ def run_gpu(args, w):
 
     if rank == 0:
         cpu_s, sample = oracle_step_seconds(w, budget_s=12.0) if not args.no_cpu else (float("nan"), "skipped")
+        cpu_batched = None
+        if not args.no_cpu:
+            bs, bthreads, bsample = batched_cpu_step_seconds(w)
+            cpu_batched = {"value": 1.0 / bs, "unit": "steps/s", "cores": bthreads, "kind": "batched fp32 (torch CPU)",
+                           "sample": bsample}
         line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -408,6 +461,7 @@ def run_gpu(args, w):
                 "kernels": per_kernel,
                 "cpu_baseline": {"value": 1.0 / cpu_s if cpu_s == cpu_s else None, "unit": "steps/s", "cores": 1,
                                  "kind": "oracle", "sample": sample},
+                "cpu_batched": cpu_batched,
                 "e2e": e2e,
                 "scoring": scoring,
                 "gpu_launches": launches,
