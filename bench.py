@@ -56,7 +56,7 @@ def _peaks():
 # by the sha256 of the kernel source it was taken on: (bytes per launch per request, note).
 # A kernel source without an entry reports traffic null.
 _ATTN_TRAFFIC = {
-    "0d1b10b1eb91989f": (99.43e6 / 4, "ncu 4-request capture (profiles/ncu_k_ctx_attn_4req.md), "
+    "4f10361a3bd242c5": (99.6e6 / 4, "ncu 4-request capture (profiles/ncu_k_ctx_attn_4req.md), "
                                        "scaled by the number of requests"),
 }
 
