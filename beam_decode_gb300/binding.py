@@ -38,7 +38,7 @@ KERNEL_NAMES = ["attn", "logsoftmax_gather", "topk_select", "advance", "results"
 # exported symbols of include/grbeam.h
 SYMBOLS = [
     "gr_trie_device_bytes", "gr_trie_create", "gr_trie_destroy",
-    "gr_beam_workspace_bytes", "gr_beam_kv_bytes", "gr_beam_create", "gr_beam_destroy",
+    "gr_beam_workspace_bytes", "gr_beam_kv_bytes", "gr_attn_schedule", "gr_beam_create", "gr_beam_destroy",
     "gr_beam_rows", "gr_beam_step", "gr_beam_request_step", "gr_beam_kv_slot", "gr_beam_kv_slot_request",
     "gr_decode_attn", "gr_constrained_topk", "gr_beam_advance", "gr_beam_rewind", "gr_beam_admit",
     "gr_beam_set_graph_mode", "gr_beam_sync", "gr_beam_results", "gr_beam_path", "gr_beam_status",
@@ -105,6 +105,8 @@ def lib() -> ctypes.CDLL:
             "gr_trie_destroy": [vp],
             "gr_beam_workspace_bytes": [P(GrConfig), P(GrRequest), c_int, P(sz)],
             "gr_beam_kv_bytes": [P(GrConfig), P(GrRequest), c_int, P(sz)],
+            "gr_attn_schedule": [P(GrConfig), vp, vp, c_int, c_int, P(c_int), P(c_int), P(c_int), vp, c_int, vp,
+                                 c_int, vp, c_int],
             "gr_beam_create": [P(GrConfig), P(GrRequest), c_int, P(GrBuffers), vp, P(vp)],
             "gr_beam_destroy": [vp],
             "gr_beam_rows": [vp, P(c_int), vp],
@@ -151,6 +153,29 @@ def check(status: int) -> None:
     if status != GR_OK:
         L = lib()
         raise GrError(status, L.gr_status_str(status).decode(), L.gr_last_error().decode())
+
+
+def attn_schedule(n_q_heads: int, n_kv_heads: int, ctx_lens: Sequence[int], widths: Sequence[int],
+                  n_sm: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """The attention schedule of a batch (gr_attn_schedule), host only: (units [n, 7], jobs [n, 4],
+    ctas [n, 2]) int32 arrays with the columns the header lists."""
+    L = lib()
+    cfg = GrConfig(n_layers=1, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=128, vocab=1, code_base=0,
+                   n_levels=1, codes_per_level=1, pool_tokens=1)
+    cl = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    bw = np.ascontiguousarray(widths, dtype=np.int32)
+    nu, nj, nc = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = L.gr_attn_schedule(ctypes.byref(cfg), cl.ctypes.data, bw.ctypes.data, len(cl), n_sm, ctypes.byref(nu),
+                            ctypes.byref(nj), ctypes.byref(nc), None, 0, None, 0, None, 0)
+    if st not in (GR_OK, GR_ERR_CAPACITY):
+        check(st)
+    units = np.zeros((nu.value, 7), np.int32)
+    jobs = np.zeros((nj.value, 4), np.int32)
+    ctas = np.zeros((nc.value, 2), np.int32)
+    check(L.gr_attn_schedule(ctypes.byref(cfg), cl.ctypes.data, bw.ctypes.data, len(cl), n_sm, ctypes.byref(nu),
+                             ctypes.byref(nj), ctypes.byref(nc), units.ctypes.data, len(units), jobs.ctypes.data,
+                             len(jobs), ctas.ctypes.data, len(ctas)))
+    return units, jobs, ctas
 
 
 def _stream_ptr(stream=None) -> ctypes.c_void_p:

@@ -640,6 +640,54 @@ extern "C" gr_status gr_beam_workspace_bytes(const gr_config* cfg, const gr_requ
     return GR_OK;
 }
 
+extern "C" gr_status gr_attn_schedule(const gr_config* cfg, const int* ctx_len, const int* beam_width,
+                                      int n_requests, int n_sm, int* n_units, int* n_jobs, int* n_ctas,
+                                      int32_t* units, int max_units, int32_t* jobs, int max_jobs, int32_t* ctas,
+                                      int max_ctas) {
+    if (cfg == nullptr || ctx_len == nullptr || beam_width == nullptr || n_units == nullptr || n_jobs == nullptr ||
+        n_ctas == nullptr)
+        return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    if (n_requests < 1 || n_sm < 1) return fail(GR_ERR_INVALID_ARG, "n_requests and n_sm must be >= 1");
+    if (cfg->n_kv_heads < 1 || cfg->n_q_heads < cfg->n_kv_heads || cfg->n_q_heads % cfg->n_kv_heads != 0)
+        return fail(GR_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+    const int G = cfg->n_q_heads / cfg->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+        return fail(GR_ERR_UNSUPPORTED, "query heads per KV head must be 1, 2, 4, 8 or 16 (got %d)", G);
+    std::vector<gr_request> reqs(n_requests);
+    for (int r = 0; r < n_requests; ++r) {
+        if (ctx_len[r] < 1 || beam_width[r] < 1 || beam_width[r] > kMaxBeam)
+            return fail(GR_ERR_INVALID_ARG, "request %d: ctx_len >= 1 and beam_width in 1..%d", r, kMaxBeam);
+        reqs[r] = gr_request{};
+        reqs[r].ctx_len = ctx_len[r];
+        reqs[r].beam_width = beam_width[r];
+    }
+    std::vector<int> uo, nu;
+    const Schedule sc = build_schedule(cfg, reqs.data(), n_requests, n_sm, uo, nu);
+    *n_units = (int)sc.units.size();
+    *n_jobs = (int)sc.jobs.size();
+    *n_ctas = (int)sc.cta_jobs.size();
+    if (*n_units > max_units || *n_jobs > max_jobs || *n_ctas > max_ctas || units == nullptr || jobs == nullptr ||
+        ctas == nullptr)
+        return fail(GR_ERR_CAPACITY, "schedule needs %d units, %d jobs, %d CTAs", *n_units, *n_jobs, *n_ctas);
+    for (int k = 0; k < *n_units; ++k) {
+        const GrAttnUnit& u = sc.units[k];
+        const int32_t v[7] = {u.req, u.head, u.beam0, u.nqt, u.first_slot, u.n_slots, u.n_tiles};
+        for (int e = 0; e < 7; ++e) units[7 * k + e] = v[e];
+    }
+    for (int k = 0; k < *n_jobs; ++k) {
+        const GrAttnJob& j = sc.jobs[k];
+        jobs[4 * k + 0] = j.unit;
+        jobs[4 * k + 1] = j.t0;
+        jobs[4 * k + 2] = j.t1;
+        jobs[4 * k + 3] = j.slot;
+    }
+    for (int k = 0; k < *n_ctas; ++k) {
+        ctas[2 * k + 0] = sc.cta_jobs[k].x;
+        ctas[2 * k + 1] = sc.cta_jobs[k].y;
+    }
+    return GR_OK;
+}
+
 extern "C" gr_status gr_beam_kv_bytes(const gr_config* cfg, const gr_request* reqs, int n_requests, size_t* bytes) {
     if (bytes == nullptr) return fail(GR_ERR_INVALID_ARG, "bytes is NULL");
     gr_status s = check_config(cfg, reqs, n_requests);

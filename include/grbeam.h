@@ -150,6 +150,31 @@ gr_status gr_beam_workspace_bytes(const gr_config* cfg, const gr_request* reqs, 
 gr_status gr_beam_kv_bytes(const gr_config* cfg, const gr_request* reqs, int n_requests,
                            size_t* bytes);
 
+/* The attention schedule gr_beam_create builds for requests of these context
+ * lengths (ctx_len[r] >= 1) and beam widths (beam_width[r] in 1..1024) on a
+ * GPU with n_sm SMs.  Host only: no device, no trie, nothing allocated.
+ * Only the head counts of cfg are read.  The decode attention kernel works
+ * through this table, so it is the place to check its invariants without a
+ * GPU.
+ *
+ * A unit is up to 256 query rows (two 128-row tiles) of one (request, KV
+ * head).  Its key tiles of 128 keys are cut into contiguous ranges, the jobs,
+ * spread over CTAs in order.  A unit's jobs own the consecutive piece slots
+ * [first slot, first slot + slots); the job of the first range merges.
+ *   units [max_units][7] int32: request, KV head, first beam, query tiles,
+ *                               first slot, slots, key tiles
+ *   jobs  [max_jobs][4]  int32: unit, first key tile, end key tile, slot
+ *   ctas  [max_ctas][2]  int32: first job, end job of each CTA
+ * *n_units, *n_jobs and *n_ctas are always written.  The arrays (caller-owned
+ * host memory) are filled only when all three are large enough; otherwise
+ * GR_ERR_CAPACITY is returned.  Errors: GR_ERR_INVALID_ARG (NULL pointer,
+ * n_requests < 1, n_sm < 1, bad lengths or widths), GR_ERR_UNSUPPORTED
+ * (query heads per KV head not 1, 2, 4, 8 or 16). */
+gr_status gr_attn_schedule(const gr_config* cfg, const int* ctx_len, const int* beam_width,
+                           int n_requests, int n_sm, int* n_units, int* n_jobs, int* n_ctas,
+                           int32_t* units, int max_units, int32_t* jobs, int max_jobs,
+                           int32_t* ctas, int max_ctas);
+
 /* Validate the batch, carve the workspace, upload the request table, the
  * attention schedule and the TMA descriptors of the ContextKV pool, and put
  * every request at step 0 with one root beam of score 0 (enqueued on
