@@ -452,7 +452,7 @@ def run_gpu(args, w):
                            "beam": w.beam_widths[0], "layers": w.n_layers, "q_heads": w.n_q_heads,
                            "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "vocab": w.vocab,
                            "levels": w.n_levels, "codes": w.codes_per_level, "items": w.n_items[0],
-                           "l2": "inputs larger than L2 (ContextKV 4.6 GB)", "parallelism": f"replicas{world}",
+                           "l2": "inputs larger than L2 (ContextKV %.2f GB)" % (batch.ctx_bytes_per_layer() * w.n_layers / 1e9), "parallelism": f"replicas{world}",
                            "cuda_graph": not args.no_graph},
                 "eager": {"value": job_value(ms_eager / args.steps, world), "unit": "steps/s",
                           "ms_per_step": ms_eager / args.steps},
