@@ -1,7 +1,7 @@
 """gr_decode_attn against the oracle's naive per-beam attention.
 
 Shapes span several 128-key tiles with ragged tails, one and two query tiles
-per unit, GQA groups 1..8, head_dim 64 and 128, BeamKV depth t = 1 and 2,
+per unit, GQA groups 1..16, head_dim 64 and 128, BeamKV depth t = 1 and 2,
 and several requests sharing one ContextKV pool.  Tolerance:
 |gpu - ref| <= 1e-2 + 1e-2*|ref| (bf16 K/V, fp32 accumulate).
 """
@@ -33,7 +33,7 @@ def test_context_lengths(T, D):
     assert max(r["worst"] for r in res) <= 1.0, res
 
 
-@pytest.mark.parametrize("G,W", [(1, 256), (2, 200), (4, 64), (8, 16), (2, 256)])
+@pytest.mark.parametrize("G,W", [(1, 256), (2, 200), (4, 64), (8, 16), (2, 256), (16, 8), (16, 24)])
 def test_groups_and_widths(G, W):
     Hkv = 2
     spec = Spec(n_q_heads=G * Hkv, n_kv_heads=Hkv, head_dim=128, vocab=2048, n_levels=2, codes_per_level=256,
