@@ -133,8 +133,10 @@ class OracleBeam:
         lse_in  optional per-beam log-sum-exp to use instead of the oracle's
                 own (float32 values; only meaningful with key_mode="f32")
         Returns a dict with per-beam ``lse`` (float64 unless overridden),
-        ``logprobs`` [n_live, C] float64 (-inf where invalid), the ordered
-        candidate list and the selection.
+        ``logprobs`` [n_live, C] float64 -- the level's C code entries of each
+        row's full-vocabulary log-softmax, for every code, valid or not (the
+        candidate list says which codes are valid) -- the ordered candidate
+        list and the selection.
         """
         t = self.t
         if t >= self.n_levels:

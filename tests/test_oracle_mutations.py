@@ -212,6 +212,35 @@ def test_beam_class_mutation_is_caught(monkeypatch, golden_dir, cls):
     assert _fails(_beam_pins(golden_dir)), cls.__name__
 
 
+# -- float32 key mutations ---------------------------------------------------------
+
+def _key_one_rounding(score32, x32, lse32):
+    # the exact S + x - LSE (float64 is exact at these magnitudes) rounded once
+    return np.float32(float(score32) + (float(x32) - float(lse32)))
+
+
+def _key_other_association(score32, x32, lse32):
+    return np.float32(np.float32(np.float32(score32) + np.float32(x32)) - np.float32(lse32))
+
+
+def _key_drops_score(score32, x32, lse32):
+    return np.float32(np.float32(x32) - np.float32(lse32))
+
+
+def _key_pins(golden_dir):
+    return [T_ls.test_key_f32_is_two_roundings_of_exact_values] + _beam_pins(golden_dir)
+
+
+@pytest.mark.parametrize("name,fn", [
+    ("key rounded once", _key_one_rounding),
+    ("key summed in the other order", _key_other_association),
+    ("key without the beam score", _key_drops_score),
+])
+def test_key_f32_mutation_is_caught(monkeypatch, golden_dir, name, fn):
+    monkeypatch.setattr(obs, "key_f32", fn)
+    assert _fails(_key_pins(golden_dir)), name
+
+
 # -- multi-item scoring mutations ---------------------------------------------------
 
 import oracle.scoring as osc
