@@ -282,7 +282,7 @@ struct Caps {
 
 struct WsLayout {
     size_t req, row_req, req_step, n_beams, parent, token, node, score, path, cand, sel_parent, sel_code, sel_key, n_sel,
-        status, tmaps, jobs, cta_jobs, units, tables_end, o_part, lse_part, piece_flag, res_codes, res_items, res_scores,
+        status, key_range, tmaps, jobs, cta_jobs, units, tables_end, o_part, lse_part, piece_flag, res_codes, res_items, res_scores,
         total;
 };
 
@@ -465,6 +465,7 @@ WsLayout ws_layout(const gr_config* c, int n, int rows, const Caps& k) {
     w.sel_key = take(4ull * rows);
     w.n_sel = take(4ull * n);
     w.status = take(16);
+    w.key_range = take(8ull * n);
     w.o_part = take(4ull * k.jobs * kUnitRows * c->head_dim);
     w.lse_part = take(4ull * k.jobs * kUnitRows);
     w.piece_flag = take(4ull * k.jobs * kUnitRows);
@@ -763,6 +764,7 @@ extern "C" gr_status gr_beam_create(const gr_config* cfg, const gr_request* reqs
         st.sel_key = reinterpret_cast<float*>(ws + w.sel_key);
         st.n_sel = reinterpret_cast<int32_t*>(ws + w.n_sel);
         st.status = reinterpret_cast<int32_t*>(ws + w.status);
+        st.key_range = reinterpret_cast<uint32_t*>(ws + w.key_range);
         st.tmaps = reinterpret_cast<CUtensorMap*>(ws + w.tmaps);
         st.jobs = reinterpret_cast<GrAttnJob*>(ws + w.jobs);
         st.cta_jobs = reinterpret_cast<int2*>(ws + w.cta_jobs);

@@ -56,8 +56,7 @@ def _peaks():
 # by the sha256 of the kernel source it was taken on: (bytes per launch per request, note).
 # A kernel source without an entry reports traffic null.
 _ATTN_TRAFFIC = {
-    "4f10361a3bd242c5": (99.6e6 / 4, "ncu 4-request capture (profiles/ncu_k_ctx_attn_4req.md), "
-                                       "scaled by the number of requests"),
+    "4f10361a3bd242c5": (99.6e6 / 4, "ncu capture of the 4-request case, scaled by the number of requests"),
 }
 
 

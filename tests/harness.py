@@ -132,13 +132,19 @@ class LockStep:
         """Run gr_decode_attn for `layer` at the current step; compare with the oracle.
         Returns the max violation ratio (<= 1 passes) and sizes compared."""
         torch = self.torch
-        s, t = self.spec, self.t
+        t = self.t
         self.write_beam_kv(t, layer)
         q = self.queries(t, layer)
         gq = torch.from_numpy(q).to(torch.bfloat16).to(self.device)
         gout = torch.full_like(gq, float("nan"))
         self.beam.decode_attn(layer, gq, gout)
-        out = gout.float().cpu().numpy()
+        return self.compare_attention(layer, q, gout.float().cpu().numpy(), requests, beams_per_request)
+
+    def compare_attention(self, layer: int, q: np.ndarray, out: np.ndarray, requests=None,
+                          beams_per_request=None) -> Dict:
+        """Element-wise check of one layer's attention output `out` [rows, Hq, D] against the
+        oracle's float64 attention at the current step (the oracle's own beams and ancestry)."""
+        s, t = self.spec, self.t
         worst, n = 0.0, 0
         reqs = range(len(s.ctx_lens)) if requests is None else requests
         for r in reqs:
@@ -170,40 +176,60 @@ class LockStep:
         """gr_constrained_topk + gr_beam_advance vs the oracle step.
         lse_mode: pass the oracle's float32 LSE to the GPU (bit-exact contract)."""
         torch = self.torch
-        s, t = self.spec, self.t
-        x = self.logits(t)
-        R = len(s.ctx_lens)
+        s = self.spec
+        x = self.logits(self.t)
         ld = x.shape[1]
         gx = torch.from_numpy(x).to(self.device)
         lp_out = torch.full((self.beam.rows, s.codes_per_level), float("nan"), device=self.device)
         lse_out = torch.full((self.beam.rows,), float("nan"), device=self.device)
-        lse_in = None
-        oinfo = []
-        # oracle first (needs only host data); its float32 LSE is the GPU's lse_in
+        oinfo, lse32 = self.oracle_topk(x)   # oracle first: its float32 LSE is the GPU's lse_in
+        lse_in = torch.from_numpy(np.nan_to_num(lse32, nan=0.0)).to(self.device) if lse_mode else None
+        self.beam.constrained_topk(gx, ld=ld, logprobs_out=lp_out, lse_out=lse_out, lse_in=lse_in)
+        self.beam.advance()
+        return self.compare_topk(oinfo, lse_mode, lse_out.cpu().numpy(), lp_out.cpu().numpy())
+
+    def oracle_lse(self, x: np.ndarray) -> np.ndarray:
+        """The oracle's float64 log-sum-exp of every live row, rounded to float32 (NaN for
+        rows that are not live); the oracle's state does not change."""
+        from oracle import log_softmax_row
+        s = self.spec
         lse32 = np.full(self.beam.rows, np.nan, dtype=np.float32)
-        for r in range(R):
+        for r in range(len(s.ctx_lens)):
+            r0, n = self.row_off[r], self.obeams[r].n_live()
+            lse32[r0:r0 + n] = [log_softmax_row(rw)[1] for rw in x[r0:r0 + n, :s.vocab]]
+        return lse32
+
+    def oracle_topk(self, x: np.ndarray):
+        """The oracle's step on the logit rows x (all requests, under the float32 key contract
+        with its own LSE rounded to float32).  Returns (per-request step info, float32 LSE per
+        row, NaN for rows that are not live)."""
+        from oracle import log_softmax_row
+        s = self.spec
+        oinfo = []
+        lse32 = np.full(self.beam.rows, np.nan, dtype=np.float32)
+        for r in range(len(s.ctx_lens)):
             ob = self.obeams[r]
             n = ob.n_live()
             r0 = self.row_off[r]
             rows = x[r0:r0 + n, :s.vocab]
-            from oracle import log_softmax_row
             lses = [log_softmax_row(rw)[1] for rw in rows]
             lse32[r0:r0 + n] = np.array(lses, dtype=np.float32)
-            info = ob.step(rows, lse_in=lse32[r0:r0 + n] if lse_mode else None)
+            info = ob.step(rows, lse_in=lse32[r0:r0 + n])
             info["lse64"] = lses
             oinfo.append(info)
-        if lse_mode:
-            lse_in = torch.from_numpy(np.nan_to_num(lse32, nan=0.0)).to(self.device)
-        self.beam.constrained_topk(gx, ld=ld, logprobs_out=lp_out, lse_out=lse_out, lse_in=lse_in)
-        self.beam.advance()
+        return oinfo, lse32
+
+    def compare_topk(self, oinfo, lse_mode: bool, lse_g=None, lp_g=None) -> Dict:
+        """The GPU's BeamPath level t (read through gr_beam_path) against the oracle's step t:
+        parents and tokens bit for bit, scores bit for bit under lse_in; the GPU's own LSE and
+        log-probabilities (when given) within 1e-4 of float64."""
+        s, t = self.spec, self.t
         res = {"lse_err": 0.0, "lp_err": 0.0, "mismatch": [], "n_sel": []}
-        lse_g = lse_out.cpu().numpy()
-        lp_g = lp_out.cpu().numpy()
-        for r in range(R):
+        for r in range(len(s.ctx_lens)):
             info = oinfo[r]
             r0 = self.row_off[r]
             n = len(info["lse64"])
-            if not lse_mode:
+            if not lse_mode and lse_g is not None:
                 res["lse_err"] = max(res["lse_err"], float(np.max(np.abs(lse_g[r0:r0 + n] - np.array(info["lse64"])))))
                 ref_lp = info["logprobs"]
                 fin = np.zeros(ref_lp.shape, dtype=bool)  # valid (beam, code) pairs per the oracle's trie
@@ -230,6 +256,77 @@ class LockStep:
 
     def gpu_results(self, r: int):
         return self.beam.results(r)
+
+
+class GraphStep:
+    """A whole decode step -- gr_decode_attn for every layer, gr_constrained_topk (with the
+    oracle's float32 LSE through lse_in) and gr_beam_advance -- captured once as a CUDA graph
+    in graph mode and replayed for the later steps, each replay checked against the oracle.
+
+    Before a replay the host writes the step's inputs into the captured buffers: the BeamKV
+    level of the codes chosen at the previous step (straight into the pool, as a model
+    would), the queries of every layer, the logits and the LSE.  The oracle sees the same
+    host arrays and keeps its own beams, ancestry and BeamKV copy."""
+
+    def __init__(self, ls: LockStep):
+        torch = ls.torch
+        assert ls.t == 1, "capture after level 0 (the first step with attention)"
+        self.ls = ls
+        s, beam = ls.spec, ls.beam
+        qs = (beam.rows, s.n_q_heads, s.head_dim)
+        self.q = [torch.zeros(qs, dtype=torch.bfloat16, device=ls.device) for _ in range(s.n_layers)]
+        self.out = [torch.zeros(qs, dtype=torch.bfloat16, device=ls.device) for _ in range(s.n_layers)]
+        self.x = torch.zeros((beam.rows, s.vocab + s.ld_pad), device=ls.device)
+        self.lse = torch.zeros((beam.rows,), device=ls.device)
+        # one eager step first (one-time kernel set-up happens outside the capture), rewound
+        self._enqueue()
+        beam.rewind(1)
+        torch.cuda.synchronize()
+        beam.set_graph_mode(True)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._enqueue()
+
+    def _enqueue(self):
+        beam = self.ls.beam
+        for layer in range(self.ls.spec.n_layers):
+            beam.decode_attn(layer, self.q[layer], self.out[layer])
+        beam.constrained_topk(self.x, ld=self.x.shape[1], lse_in=self.lse)
+        beam.advance()
+
+    def replay(self) -> Dict:
+        """Replay the graph for the current step t and compare it with the oracle: every
+        layer's attention element-wise, then the selection bit for bit."""
+        ls, torch = self.ls, self.ls.torch
+        s, t, beam = ls.spec, ls.t, ls.beam
+        shp = (beam.rows, s.n_kv_heads, s.head_dim)
+        qs = []
+        for layer in range(s.n_layers):
+            k = wl.round_to_bf16(wl.host_normal(shp, s.seed, wl.TAG_BEAM_K, sub=(t, layer)))
+            v = wl.round_to_bf16(wl.host_normal(shp, s.seed, wl.TAG_BEAM_V, sub=(t, layer)))
+            beam.beam_k[layer, t - 1].copy_(torch.from_numpy(k).to(torch.bfloat16))
+            beam.beam_v[layer, t - 1].copy_(torch.from_numpy(v).to(torch.bfloat16))
+            ls.obk[layer][t - 1], ls.obv[layer][t - 1] = k, v
+            q = ls.queries(t, layer)
+            self.q[layer].copy_(torch.from_numpy(q).to(torch.bfloat16))
+            self.out[layer].fill_(float("nan"))
+            qs.append(q)
+        x = ls.logits(t)
+        self.x.copy_(torch.from_numpy(x))
+        self.lse.copy_(torch.from_numpy(np.nan_to_num(ls.oracle_lse(x), nan=0.0)))
+        torch.cuda.synchronize()
+        self.graph.replay()
+        torch.cuda.synchronize()
+        # attention against the oracle's state before its top-K step of level t
+        worst = 0.0
+        for layer in range(s.n_layers):
+            a = ls.compare_attention(layer, qs[layer], self.out[layer].float().cpu().numpy())
+            worst = max(worst, a["worst"])
+        oinfo, _ = ls.oracle_topk(x)
+        beam.sync()   # the host's copy of the device step state, for gr_beam_path
+        res = ls.compare_topk(oinfo, lse_mode=True)
+        res["worst"] = worst
+        return res
 
 
 @dataclasses.dataclass

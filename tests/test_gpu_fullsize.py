@@ -110,3 +110,61 @@ def test_fullsize_topk_and_attention(full):
         assert np.array_equal(par, np.array(obs[r].parents[1]))
         assert np.array_equal(tok - w.code_base - w.codes_per_level, np.array(obs[r].codes[1]))
     assert beam.status() == 0
+
+
+def test_fullsize_captured_step_matches_oracle(full):
+    """The benchmark's own captured graph (bench.DeviceBatch.capture: rewind to step 1, 28
+    attention layers, the top-K with the GPU's own LSE, advance), replayed once and checked
+    against the oracle: sampled attention rows of the first and last layer for the first and
+    last request, and every request's selection at level 1."""
+    import torch
+    from oracle import beam_attention, log_softmax_row
+    w, b = full
+    beam = b.beam
+    obs = _oracle_beams(w, b.items)
+    ro = beam.row_offsets
+    # level 0 as in the benchmark's set-up, with the oracle's LSE so both sides hold the same beams
+    beam.rewind(0)
+    x0 = b.logits[0].cpu().numpy()
+    lse0 = np.zeros(b.rows, dtype=np.float32)
+    for r in range(w.n_requests):
+        lse0[ro[r]] = np.float32(log_softmax_row(x0[ro[r]])[1])
+        obs[r].step(x0[ro[r]][None], lse_in=[lse0[ro[r]]])
+    beam.constrained_topk(b.logits[0], lse_in=torch.from_numpy(lse0).cuda())
+    beam.advance()
+    for l in range(w.n_layers):
+        k, v = beam.kv_slot(l)
+        k.copy_(b.new_k[l])
+        v.copy_(b.new_v[l])
+    b.capture()
+    for l in range(w.n_layers):
+        b.out[l].fill_(float("nan"))
+    b.graph.replay()
+    torch.cuda.synchronize()
+    b.release()
+    assert beam.status() == 0
+    worst = 0.0
+    for l in (0, w.n_layers - 1):
+        out = b.out[l].float().cpu().numpy()
+        q = b.q[l].float().cpu().numpy()
+        nk = b.new_k[l].float().cpu().numpy()
+        nv = b.new_v[l].float().cpu().numpy()
+        for r in (0, w.n_requests - 1):
+            T, o0, r0, W = w.ctx_lens[r], int(b.ctx_off[r]), ro[r], w.beam_widths[r]
+            ck = b.ctx_k[l, :, o0:o0 + T].float().cpu().numpy()
+            cv = b.ctx_v[l, :, o0:o0 + T].float().cpu().numpy()
+            beams = [0, 5, 127, 128, 129, 250, obs[r].n_live() - 1]
+            ref = beam_attention(q[r0:r0 + W], ck, cv, [nk[r0:r0 + W]], [nv[r0:r0 + W]], obs[r].ancestry(),
+                                 beams=beams)
+            got = out[r0 + np.array(beams)]
+            worst = max(worst, float(np.max(np.abs(got - ref) / (ATOL + RTOL * np.abs(ref)))))
+    assert worst <= 1.0, worst
+    # level 1 from the GPU's own LSE: the same selection as the oracle's
+    x1 = b.logits[1].cpu().numpy()
+    for r in range(w.n_requests):
+        n = obs[r].n_live()
+        rows = x1[ro[r]:ro[r] + n]
+        obs[r].step(rows, lse_in=np.array([log_softmax_row(rw)[1] for rw in rows], dtype=np.float32))
+        par, tok, _, _ = beam.path(r, 1)
+        assert np.array_equal(par, np.array(obs[r].parents[1])), r
+        assert np.array_equal(tok - w.code_base - w.codes_per_level, np.array(obs[r].codes[1])), r
