@@ -18,7 +18,7 @@ SRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgrbeam.so")
 UNITS = ["api.cu", "k_topk.cu", "k_attn.cu", "k_noalloc.cu"]
-HEADERS = [os.path.join(SRC, "grbeam_internal.h"), os.path.join(SRC, "topk_dev.cuh"),
+HEADERS = [os.path.join(SRC, "grbeam_internal.h"), os.path.join(SRC, "topk_dev.cuh"), os.path.join(SRC, "attn_dev.cuh"),
            os.path.join(os.path.dirname(HERE), "include", "grbeam.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
