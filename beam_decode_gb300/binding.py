@@ -42,7 +42,8 @@ SYMBOLS = [
     "gr_beam_rows", "gr_beam_step", "gr_beam_request_step", "gr_beam_kv_slot", "gr_beam_kv_slot_request",
     "gr_decode_attn", "gr_constrained_topk", "gr_beam_advance", "gr_beam_rewind", "gr_beam_admit",
     "gr_beam_set_graph_mode", "gr_beam_sync", "gr_beam_results", "gr_beam_path", "gr_beam_status",
-    "gr_beam_set_timing", "gr_beam_kernel_stats", "gr_beam_set_wait_limit",
+    "gr_beam_set_timing", "gr_beam_kernel_stats", "gr_beam_set_wait_limit", "gr_beam_set_attn_kernel",
+    "gr_beam_attn_kernel",
     "gr_constrained_topk_noalloc", "gr_status_str", "gr_last_error",
     "gr_score_workspace_bytes", "gr_score_create", "gr_score_destroy", "gr_score_rows", "gr_score_attn",
     "gr_score_labels", "gr_score_status",
@@ -105,7 +106,7 @@ def lib() -> ctypes.CDLL:
             "gr_trie_destroy": [vp],
             "gr_beam_workspace_bytes": [P(GrConfig), P(GrRequest), c_int, P(sz)],
             "gr_beam_kv_bytes": [P(GrConfig), P(GrRequest), c_int, P(sz)],
-            "gr_attn_schedule": [P(GrConfig), vp, vp, c_int, c_int, P(c_int), P(c_int), P(c_int), vp, c_int, vp,
+            "gr_attn_schedule": [P(GrConfig), vp, vp, c_int, c_int, c_int, P(c_int), P(c_int), P(c_int), vp, c_int, vp,
                                  c_int, vp, c_int],
             "gr_beam_create": [P(GrConfig), P(GrRequest), c_int, P(GrBuffers), vp, P(vp)],
             "gr_beam_destroy": [vp],
@@ -127,6 +128,8 @@ def lib() -> ctypes.CDLL:
             "gr_beam_set_timing": [vp, c_int],
             "gr_beam_kernel_stats": [vp, c_int, P(c_i64), P(ctypes.c_double), c_int],
             "gr_beam_set_wait_limit": [vp, c_i64],
+            "gr_beam_set_attn_kernel": [vp, c_int, vp],
+            "gr_beam_attn_kernel": [vp, P(c_int)],
             "gr_constrained_topk_noalloc": [vp, c_i64, c_int, c_int, c_int, c_int, vp, vp, c_int, vp, vp, vp, vp,
                                             vp],
             "gr_score_workspace_bytes": [P(GrScoreConfig), P(GrScoreRequest), c_int, P(sz)],
@@ -156,23 +159,24 @@ def check(status: int) -> None:
 
 
 def attn_schedule(n_q_heads: int, n_kv_heads: int, ctx_lens: Sequence[int], widths: Sequence[int],
-                  n_sm: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+                  n_sm: int, head_dim: int = 128, attn_kernel: int = 0) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     """The attention schedule of a batch (gr_attn_schedule), host only: (units [n, 7], jobs [n, 4],
-    ctas [n, 2]) int32 arrays with the columns the header lists."""
+    ctas [n, 2]) int32 arrays with the columns the header lists.  attn_kernel: 0 automatic (the
+    single-CTA kernel), 1 single-CTA, 2 the CTA-pair kernel (ctas are then CTA pairs)."""
     L = lib()
-    cfg = GrConfig(n_layers=1, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=128, vocab=1, code_base=0,
+    cfg = GrConfig(n_layers=1, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim, vocab=1, code_base=0,
                    n_levels=1, codes_per_level=1, pool_tokens=1)
     cl = np.ascontiguousarray(ctx_lens, dtype=np.int32)
     bw = np.ascontiguousarray(widths, dtype=np.int32)
     nu, nj, nc = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    st = L.gr_attn_schedule(ctypes.byref(cfg), cl.ctypes.data, bw.ctypes.data, len(cl), n_sm, ctypes.byref(nu),
+    st = L.gr_attn_schedule(ctypes.byref(cfg), cl.ctypes.data, bw.ctypes.data, len(cl), n_sm, attn_kernel, ctypes.byref(nu),
                             ctypes.byref(nj), ctypes.byref(nc), None, 0, None, 0, None, 0)
     if st not in (GR_OK, GR_ERR_CAPACITY):
         check(st)
     units = np.zeros((nu.value, 7), np.int32)
     jobs = np.zeros((nj.value, 4), np.int32)
     ctas = np.zeros((nc.value, 2), np.int32)
-    check(L.gr_attn_schedule(ctypes.byref(cfg), cl.ctypes.data, bw.ctypes.data, len(cl), n_sm, ctypes.byref(nu),
+    check(L.gr_attn_schedule(ctypes.byref(cfg), cl.ctypes.data, bw.ctypes.data, len(cl), n_sm, attn_kernel, ctypes.byref(nu),
                              ctypes.byref(nj), ctypes.byref(nc), units.ctypes.data, len(units), jobs.ctypes.data,
                              len(jobs), ctas.ctypes.data, len(ctas)))
     return units, jobs, ctas
@@ -359,6 +363,15 @@ class Beam:
 
     def set_wait_limit(self, ns: int) -> None:
         check(lib().gr_beam_set_wait_limit(self.handle, ns))
+
+    def set_attn_kernel(self, mode: int) -> None:
+        """0 automatic, 1 the single-CTA attention kernel, 2 the CTA-pair kernel (between steps)."""
+        check(lib().gr_beam_set_attn_kernel(self.handle, mode, _stream_ptr()))
+
+    def attn_kernel(self) -> str:
+        v = ctypes.c_int(0)
+        check(lib().gr_beam_attn_kernel(self.handle, ctypes.byref(v)))
+        return "pair" if v.value else "single"
 
 
 class Score:

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgrbeam.so")
-UNITS = ["api.cu", "k_topk.cu", "k_attn.cu", "k_noalloc.cu"]
+UNITS = ["api.cu", "k_topk.cu", "k_attn.cu", "k_attn_pair.cu", "k_noalloc.cu"]
 HEADERS = [os.path.join(SRC, "grbeam_internal.h"), os.path.join(SRC, "topk_dev.cuh"), os.path.join(SRC, "attn_dev.cuh"),
            os.path.join(os.path.dirname(HERE), "include", "grbeam.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -322,7 +322,7 @@ gr_status check_config(const gr_config* c, const gr_request* reqs, int n) {
 // Attention schedule: units of <= 256 query rows per (request, KV head);
 // their key tiles are cut into ~equal contiguous ranges, one per CTA.
 Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n_sm,
-                        std::vector<int>& unit_off, std::vector<int>& n_ub) {
+                        std::vector<int>& unit_off, std::vector<int>& n_ub, bool pair = false) {
     Schedule s;
     const int G = c->n_q_heads / c->n_kv_heads;
     const int bpu = kUnitRows / G;
@@ -348,7 +348,8 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     }
     int64_t tiles_all = 0;
     for (auto& u : s.units) tiles_all += u.n_tiles;
-    const int n_cta = (int)std::min<int64_t>(std::max(n_sm, 1), tiles_all);
+    // the pair kernel runs one unit on a CTA pair: its "CTAs" below are pairs
+    const int n_cta = (int)std::min<int64_t>(std::max(pair ? n_sm / 2 : n_sm, 1), tiles_all);
     // Cost model of a CTA's time (measured on the attention kernel at ctx 5000, in units of
     // ~83 ns): a key tile costs 20 with two query tiles (they ping-pong) and 17 with one;
     // every job after a CTA's first costs kSwitch more (publish, the next job's Q, pipeline
@@ -358,8 +359,11 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     // neighbouring CTAs), a unit cut where a CTA's budget runs out.  A cut unit's first range
     // is then the last job of its CTA and its later ranges are the first jobs of the next
     // CTAs, which publish them before they wait for anything.
-    constexpr int64_t kSwitch = 36, kMerge = 105;
-    auto tile_cost = [](const GrAttnUnit& u) -> int64_t { return u.nqt == 2 ? 20 : 17; };
+    // The pair kernel (cost in the same units): a key tile costs a pair 7 with one or two
+    // query tiles (each CTA computes its 128 rows of an M = 256 MMA), a job switch 30, a
+    // merge 100.
+    const int64_t kSwitch = pair ? 30 : 36, kMerge = pair ? 100 : 105;
+    auto tile_cost = [pair](const GrAttnUnit& u) -> int64_t { return pair ? 7 : (u.nqt == 2 ? 20 : 17); };
     // returns the CTAs used (n_cta + 1: does not fit); with emit, writes jobs and ranges
     auto walk = [&](int64_t T, bool emit) -> int {
         int cta = 0, njobs = 0, job_begin = 0;
@@ -421,6 +425,11 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     return s;
 }
 
+// Which decode-attention kernel a batch runs: mode 2 the CTA-pair kernel (head_dim 128),
+// otherwise the single-CTA kernel.  The automatic choice (mode 0) is the single-CTA kernel:
+// on the measured workloads (contexts 1000..5000, beams 30..256) it is the faster of the two.
+bool choose_pair(const gr_config* c, int mode) { return c->head_dim == 128 && mode == 2; }
+
 // Each unit gets its request's fixed fields, and each job a copy of its unit: starting a
 // job on the device then takes one table read.
 void finalize_jobs(Schedule& s, const GrReqDev* rq) {
@@ -446,7 +455,7 @@ WsLayout ws_layout(const gr_config* c, int n, int rows, const Caps& k) {
     // tables (uploaded at create and at every admission) come first
     w.req = take(sizeof(GrReqDev) * n);
     w.row_req = take(4ull * rows);
-    w.tmaps = take(sizeof(CUtensorMap) * 2 * n, 128);
+    w.tmaps = take(sizeof(CUtensorMap) * kTmapsPerReq * n, 128);
     w.jobs = take(sizeof(GrAttnJob) * k.jobs);
     w.cta_jobs = take(sizeof(int2) * k.ctas);
     w.units = take(sizeof(GrAttnUnit) * k.units);
@@ -519,6 +528,7 @@ struct gr_beam {
     std::vector<Ev> events[GR_KERNEL_KINDS];
     std::vector<Ev> event_pool;
     int64_t wait_limit_ns = 2000000000ll;
+    int attn_mode = 0;            // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel
 
     int levels(int r) const { return reqs[r].trie->n_levels; }
     bool decoding(int r) const { return req_step[r] < levels(r); }
@@ -574,7 +584,8 @@ gr_status status_from_word(int w) {
 gr_status build_tables(gr_beam* h) {
     const gr_config* cfg = &h->cfg;
     std::vector<int> unit_off, n_ub;
-    Schedule sc = build_schedule(cfg, h->reqs.data(), h->n_req, h->n_sm, unit_off, n_ub);
+    const bool pair = choose_pair(cfg, h->attn_mode);
+    Schedule sc = build_schedule(cfg, h->reqs.data(), h->n_req, h->n_sm, unit_off, n_ub, pair);
     if (sc.units.size() > h->caps.units || sc.jobs.size() > h->caps.jobs || sc.cta_jobs.size() > h->caps.ctas)
         return fail(GR_ERR_CAPACITY, "attention schedule exceeds the workspace's tables");
     h->sched = std::move(sc);
@@ -611,12 +622,15 @@ gr_status build_tables(gr_beam* h) {
         const uint64_t off = (uint64_t)q.ctx_offset * D * 2;
         const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)cfg->pool_tokens * D * 2;
         gr_status s;
-        if ((s = make_tmap_3d(&tm[2 * r], static_cast<const uint8_t*>(h->bufs.ctx_k) + off, D, q.ctx_len, zdim, s1, s2,
-                              64, kTileKeys, 1)) != GR_OK ||
-            (s = make_tmap_3d(&tm[2 * r + 1], static_cast<const uint8_t*>(h->bufs.ctx_v) + off, D, q.ctx_len, zdim, s1,
-                              s2, 64, kTileKeys, 1)) != GR_OK)
+        CUtensorMap* m = tm + kTmapsPerReq * r;
+        const uint8_t* kb = static_cast<const uint8_t*>(h->bufs.ctx_k) + off;
+        if ((s = make_tmap_3d(&m[0], kb, D, q.ctx_len, zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK ||
+            (s = make_tmap_3d(&m[1], static_cast<const uint8_t*>(h->bufs.ctx_v) + off, D, q.ctx_len, zdim, s1, s2, 64,
+                              kTileKeys, 1)) != GR_OK ||
+            (s = make_tmap_3d(&m[2], kb, D, q.ctx_len, zdim, s1, s2, 64, kTileKeys / 2, 1)) != GR_OK)
             return s;
     }
+    h->st.attn_pair = pair ? 1 : 0;
     finalize_jobs(h->sched, rq);
     memcpy(img + w.jobs, h->sched.jobs.data(), sizeof(GrAttnJob) * h->sched.jobs.size());
     memcpy(img + w.cta_jobs, h->sched.cta_jobs.data(), sizeof(int2) * h->sched.cta_jobs.size());
@@ -642,13 +656,16 @@ extern "C" gr_status gr_beam_workspace_bytes(const gr_config* cfg, const gr_requ
 }
 
 extern "C" gr_status gr_attn_schedule(const gr_config* cfg, const int* ctx_len, const int* beam_width,
-                                      int n_requests, int n_sm, int* n_units, int* n_jobs, int* n_ctas,
+                                      int n_requests, int n_sm, int attn_kernel, int* n_units, int* n_jobs, int* n_ctas,
                                       int32_t* units, int max_units, int32_t* jobs, int max_jobs, int32_t* ctas,
                                       int max_ctas) {
     if (cfg == nullptr || ctx_len == nullptr || beam_width == nullptr || n_units == nullptr || n_jobs == nullptr ||
         n_ctas == nullptr)
         return fail(GR_ERR_INVALID_ARG, "NULL argument");
     if (n_requests < 1 || n_sm < 1) return fail(GR_ERR_INVALID_ARG, "n_requests and n_sm must be >= 1");
+    if (attn_kernel < 0 || attn_kernel > 2) return fail(GR_ERR_INVALID_ARG, "attn_kernel must be 0, 1 or 2");
+    if (attn_kernel == 2 && cfg->head_dim != 128)
+        return fail(GR_ERR_UNSUPPORTED, "the CTA-pair kernel needs head_dim 128 (got %d)", cfg->head_dim);
     if (cfg->n_kv_heads < 1 || cfg->n_q_heads < cfg->n_kv_heads || cfg->n_q_heads % cfg->n_kv_heads != 0)
         return fail(GR_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
     const int G = cfg->n_q_heads / cfg->n_kv_heads;
@@ -663,7 +680,7 @@ extern "C" gr_status gr_attn_schedule(const gr_config* cfg, const int* ctx_len, 
         reqs[r].beam_width = beam_width[r];
     }
     std::vector<int> uo, nu;
-    const Schedule sc = build_schedule(cfg, reqs.data(), n_requests, n_sm, uo, nu);
+    const Schedule sc = build_schedule(cfg, reqs.data(), n_requests, n_sm, uo, nu, choose_pair(cfg, attn_kernel));
     *n_units = (int)sc.units.size();
     *n_jobs = (int)sc.jobs.size();
     *n_ctas = (int)sc.cta_jobs.size();
@@ -885,8 +902,10 @@ extern "C" gr_status gr_decode_attn(gr_beam* h, int layer, const void* q, void* 
     cudaStream_t cs = (cudaStream_t)stream;
     const int64_t lim = h->wait_limit_ns;
     if ((s = run_kernel(h, GR_KERNEL_ATTN, cs, [&] {
-             return launch_ctx_attn(h->st, qmap, layer, static_cast<const uint16_t*>(q), static_cast<uint16_t*>(out),
-                                    lim, cs);
+             const uint16_t* qq = static_cast<const uint16_t*>(q);
+             uint16_t* oo = static_cast<uint16_t*>(out);
+             return h->st.attn_pair ? launch_pair_attn(h->st, qmap, layer, qq, oo, lim, cs)
+                                    : launch_ctx_attn(h->st, qmap, layer, qq, oo, lim, cs);
          })) != GR_OK)
         return s;
     if (!h->graph_mode) h->attn_done[layer] = 1;
@@ -985,6 +1004,33 @@ extern "C" gr_status gr_beam_set_graph_mode(gr_beam* h, int enable) {
     if (enable && (h->topk_done || std::any_of(h->attn_done.begin(), h->attn_done.end(), [](uint8_t d) { return d; })))
         return fail(GR_ERR_STATE, "graph mode starts between steps");
     h->graph_mode = enable != 0;
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_set_attn_kernel(gr_beam* h, int mode, gr_stream_t stream) {
+    if (h == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL handle");
+    if (mode < 0 || mode > 2) return fail(GR_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
+    if (mode == 2 && h->cfg.head_dim != 128) return fail(GR_ERR_UNSUPPORTED, "the CTA-pair kernel needs head_dim 128");
+    if (h->graph_mode) return fail(GR_ERR_STATE, "the attention kernel changes outside graph mode");
+    if (h->topk_done || std::any_of(h->attn_done.begin(), h->attn_done.end(), [](uint8_t d) { return d != 0; }))
+        return fail(GR_ERR_STATE, "the attention kernel changes between steps");
+    const int keep = h->attn_mode;
+    h->attn_mode = mode;
+    gr_status s = build_tables(h);
+    if (s != GR_OK) {
+        h->attn_mode = keep;
+        build_tables(h);
+        return s;
+    }
+    cudaStream_t cs = (cudaStream_t)stream;
+    GR_CUDA(cudaMemcpyAsync(h->bufs.workspace, h->img.data(), h->img.size(), cudaMemcpyHostToDevice, cs),
+            "attention kernel tables");
+    return GR_OK;
+}
+
+extern "C" gr_status gr_beam_attn_kernel(const gr_beam* h, int* pair) {
+    if (h == nullptr || pair == nullptr) return fail(GR_ERR_INVALID_ARG, "NULL argument");
+    *pair = h->st.attn_pair;
     return GR_OK;
 }
 
@@ -1187,7 +1233,7 @@ ScoreLayout score_layout(int n, int rows, int n_cand, int n_labels, int head_dim
         return r;
     };
     w.req = take(sizeof(GrReqDev) * n);
-    w.tmaps = take(sizeof(CUtensorMap) * 2 * n, 128);
+    w.tmaps = take(sizeof(CUtensorMap) * kTmapsPerReq * n, 128);
     w.jobs = take(sizeof(GrAttnJob) * k.jobs);
     w.cta_jobs = take(sizeof(int2) * k.ctas);
     w.units = take(sizeof(GrAttnUnit) * k.units);
@@ -1329,10 +1375,11 @@ extern "C" gr_status gr_score_create(const gr_score_config* cfg, const gr_score_
                 }
             const uint64_t off = (uint64_t)reqs[r].ctx_offset * D * 2;
             const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)cfg->pool_tokens * D * 2;
-            if ((s = make_tmap_3d(&tm[2 * r], static_cast<const uint8_t*>(bufs->ctx_k) + off, D, reqs[r].ctx_len, zdim,
-                                  s1, s2, 64, kTileKeys, 1)) != GR_OK ||
-                (s = make_tmap_3d(&tm[2 * r + 1], static_cast<const uint8_t*>(bufs->ctx_v) + off, D, reqs[r].ctx_len,
-                                  zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK) {
+            // the scoring pass runs the single-CTA kernel, which reads the first two maps
+            if ((s = make_tmap_3d(&tm[kTmapsPerReq * r], static_cast<const uint8_t*>(bufs->ctx_k) + off, D,
+                                  reqs[r].ctx_len, zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK ||
+                (s = make_tmap_3d(&tm[kTmapsPerReq * r + 1], static_cast<const uint8_t*>(bufs->ctx_v) + off, D,
+                                  reqs[r].ctx_len, zdim, s1, s2, 64, kTileKeys, 1)) != GR_OK) {
                 delete h;
                 return s;
             }

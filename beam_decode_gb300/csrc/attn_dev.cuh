@@ -69,6 +69,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// 16-byte asynchronous copy global -> shared (through L2), completed by cp_async_wait_all
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// the thread's copies have landed (they read valid global memory, so this always ends)
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // a store whose line L2 should keep (evict_last policy): a published piece waits there
 // for its merger
 __device__ __forceinline__ uint64_t l2_evict_last() {
@@ -283,13 +290,18 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
-// one thread waits for a flag written by another CTA of the same (cooperative) launch
+// one thread waits for a flag written by another CTA of the same (cooperative) launch; the
+// acquire load orders the thread's later reads of what the writer published before it
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t value, const Waiter w) {
-    const volatile uint32_t* f = reinterpret_cast<const volatile uint32_t*>(flag);
-    if (*f == value) return true;
+    if (ld_acquire_gpu(flag) == value) return true;
     const uint64_t t0 = global_timer();
     uint32_t spins = 0;
-    while (*f != value) {
+    while (ld_acquire_gpu(flag) != value) {
         if (w.limit < 0 || ((++spins) & 31) == 0) {
             if (*w.abort) return false;
             if (w.limit < 0 || (int64_t)(global_timer() - t0) > w.limit) {
@@ -357,6 +369,66 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // ---------------------------------------------------------------------------
 // the end of a job for one query row
 // ---------------------------------------------------------------------------
+// A merging warp stages its rows' private keys (BeamKV K and V rows) in its staging area,
+// kEpiSlots keys at a time: slot k holds a key's K row, its V row and one 16-byte chunk of
+// padding (against bank conflicts when the lanes read different slots).
+template <int D>
+struct EpiArea {
+    static constexpr int kSlotBytes = 4 * D + 16;
+    static constexpr int kSlots = 32;
+    static constexpr int kBytes = kSlots * kSlotBytes;  // a warp's staging area
+};
+
+// The private keys a merging warp folds in, located when its job starts: the lookups along the
+// beams' ancestry (dependent global loads) then overlap the job's key tiles instead of
+// delaying its end.  Keys are numbered warp-wide.  Decode: key (level j, beam bl of the warp's
+// beams) is j * nbw + bl.  Scoring: a key is a pool row, numbered from the warp's first one
+// (its rows' segments are consecutive pool rows).  Lane l stages key p0 + l of a batch.
+struct EpiKeys {
+    int lo;         // scoring: the warp's first pool row
+    int total;      // keys the warp stages (0: none, or the job does not merge)
+    int64_t key0;   // the BeamKV / pool row lane l stages in the first batch (-1: none)
+    int64_t key1;   // in the second batch
+};
+
+template <bool kScore>
+__device__ __forceinline__ int64_t epi_key_row(const GrState& st, const GrAttnUnit& U, int layer, int lo, int total,
+                                               int b_first, int G, int lane, int p0) {
+    const int idx = p0 + lane;
+    if (idx >= total) return -1;
+    const int L = st.n_levels;
+    if constexpr (kScore) {
+        return ((int64_t)layer * st.rows + lo + idx) * st.n_kv_heads + U.head;
+    } else {
+        const int nbw = G >= 32 ? 1 : 32 / G;  // beams the warp's rows belong to
+        const int t = st.req_step[U.req];
+        const int j = idx / nbw, b = b_first + (idx - j * nbw);
+        if (b >= U.width || b >= st.n_beams[U.req * (L + 1) + t]) return -1;
+        const int pool = U.row_off + __ldg(st.path + ((int64_t)(t - 1) * st.rows + U.row_off + b) * L + j);
+        return (((int64_t)layer * (L - 1) + j) * st.rows + pool) * st.n_kv_heads + U.head;
+    }
+}
+
+// b_first: the beam of the warp's first row (decode)
+template <int D, bool kScore>
+__device__ __forceinline__ EpiKeys epi_keys(const GrState& st, const GrAttnUnit& U, const GrAttnJob& J,
+                                            const RowInfo& ri, int layer, int b_first, int G, int lane) {
+    EpiKeys k{0, 0, -1, -1};
+    if (J.slot != U.first_slot) return k;  // a later key range publishes; it stages nothing
+    if constexpr (kScore) {
+        k.lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(ri.live ? ri.pool0 : 0x7fffffff));
+        const int hi = __reduce_max_sync(0xffffffffu, ri.live ? ri.pool0 + ri.n_priv - 1 : -1);
+        k.total = hi >= k.lo ? hi - k.lo + 1 : 0;
+    } else {
+        const int nbw = G >= 32 ? 1 : 32 / G;
+        k.total = __reduce_max_sync(0xffffffffu, ri.n_priv) * nbw;
+    }
+    constexpr int kS = EpiArea<D>::kSlots;
+    k.key0 = epi_key_row<kScore>(st, U, layer, k.lo, k.total, b_first, G, lane, 0);
+    if (k.total > kS) k.key1 = epi_key_row<kScore>(st, U, layer, k.lo, k.total, b_first, G, lane, kS);
+    return k;
+}
+
 // One row's end of a job (each softmax thread of the kernel works on its own row, all 32
 // lanes of a warp together): the row's unnormalised O over the job's key tiles, its running
 // max m_used (in score units) and sum l are
@@ -366,23 +438,53 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 //     published pieces by a log-sum-exp combine, then the row's private keys folded in one at
 //     a time (decode: the t BeamKV keys on its beam's ancestry path; scoring: its own
 //     candidate up to itself), then the bf16 output row.
-// qs is the row in the job's Q tile (128-byte rows, 64-dimension boxes of 128 rows), area the
-// warp's kArea bytes of staging space, free once wait_area() returns true; bbar the warp's
-// bulk-copy mbarrier and bcnt its phase count.  wait_o(ov) waits for the job's last PV, reads
-// the row's O into ov and frees the TMEM accumulator; merged() runs once a merging warp is
-// done with area and the Q tile.  Returns false when a wait gave up.
-template <int D, bool kScore, int kArea, class WaitO, class WaitArea, class Merged>
+// ek are the warp's keys (epi_keys at the job's start); qs is the row in the job's Q tile
+// (128-byte rows, 64-dimension boxes of 128 rows), area the warp's EpiArea<D>::kBytes of
+// staging space, free once wait_area() returns true.  wait_o(ov) waits for the job's last PV,
+// reads the row's O into ov and frees the TMEM accumulator; merged() runs once a merging warp
+// is done with area and the Q tile.  Returns false when a wait gave up.
+template <int D, bool kScore, class WaitO, class WaitArea, class Merged>
 __device__ __forceinline__ bool job_epilogue(const GrState& st, const GrAttnUnit& U, const GrAttnJob& J,
-                                             const RowInfo& ri, int prow, int row_t, int lane, int b_first,
-                                             int layer, float scale, float m_used, float l, const uint8_t* qs,
-                                             uint8_t* area, uint32_t bbar, uint32_t& bcnt, uint32_t*& pend_flag,
-                                             uint16_t* __restrict__ out, const Waiter& wt, WaitO&& wait_o,
-                                             WaitArea&& wait_area, Merged&& merged) {
+                                             const RowInfo& ri, const EpiKeys& ek, int row_t, int lane, int b_first,
+                                             int prow, int layer, float scale, float m_used, float l,
+                                             const uint8_t* qs, uint8_t* area, uint32_t*& pend_flag, uint16_t* __restrict__ out, const Waiter& wt,
+                                             WaitO&& wait_o, WaitArea&& wait_area, Merged&& merged) {
     constexpr int kQBox = 128 * 128;  // bytes between the 64-dimension boxes of a query tile
+    constexpr int kSlotBytes = EpiArea<D>::kSlotBytes;
+    constexpr int kSlots = EpiArea<D>::kSlots;
     const int G = st.n_q_heads / st.n_kv_heads;
     const bool merger = (J.slot == U.first_slot);
     const float lse_own = m_used * scale + logf(l);
     const float inv_l = 1.f / l;
+    const int nbw = G >= 32 ? 1 : 32 / G;  // beams the warp's rows belong to
+    const int bl = G >= 32 ? 0 : lane / G;  // this row's beam among them
+    const uint32_t area_s = smem_u32(area);
+    // Stage a batch: lane l's key (or none: key < 0) into slot l.  The warp copies one key per
+    // instruction (two for D = 64), each lane 16 bytes of its K or V row, so the reads of a key
+    // are contiguous.
+    auto stage = [&](int64_t key) {
+        constexpr int kCh = D / 4;          // 16-byte chunks of a key's K and V rows
+        constexpr int kPer = 32 / kCh;      // keys per instruction
+        const int sub = lane / kCh, ch = lane % kCh;
+        const uint16_t* src = (ch < D / 8 ? st.beam_k : st.beam_v) + (ch % (D / 8)) * 8;
+#pragma unroll 4
+        for (int k = 0; k < 32; k += kPer) {
+            const int64_t kk = __shfl_sync(0xffffffffu, key, k + sub);
+            if (kk >= 0) cp_async16(area_s + (k + sub) * kSlotBytes + ch * 16, src + kk * D);
+        }
+        cp_async_commit();
+    };
+    // A merging warp's first batch of keys goes out as soon as the staging area is free (the
+    // job's last key tile has been used), before its pieces and its O: the copies overlap them.
+    // A warp that gives up waits for its copies: none may land after the CTA has gone.
+    if (merger && ek.total > 0) {
+        if (!wait_area()) return false;
+        stage(ek.key0);
+    }
+    auto give_up = [&]() {
+        cp_async_wait_all();
+        return false;
+    };
     // A merging job reads its pieces' ready flags and log-sum-exps while its last PV MMAs are
     // still running: the weights of the parts are known when O arrives.
     constexpr int kPieceRegs = 4;
@@ -395,8 +497,7 @@ __device__ __forceinline__ bool job_epilogue(const GrState& st, const GrAttnUnit
         if (ri.live)
             for (int pp = 1; pp <= n_other && have; ++pp)
                 have = wait_flag(st.piece_flag + (int64_t)(U.first_slot + pp) * kUnitRows + prow, 1u, wt);
-        if (__any_sync(0xffffffffu, !have)) return false;
-        __threadfence();
+        if (__any_sync(0xffffffffu, !have)) return give_up();
         // the context part: own O and the published pieces, relative to the max M of their
         // log-sum-exps; a and den stay unnormalised until the end
 #pragma unroll
@@ -414,48 +515,8 @@ __device__ __forceinline__ bool job_epilogue(const GrState& st, const GrAttnUnit
             den += wp[pp];
         }
     }
-    // The merge copies its rows' BeamKV keys into the warp's staging area.  Keys are numbered
-    // warp-wide and staged kSlots at a time.  Decode: key (level j, beam bl of the warp's
-    // beams) is j * nbw + bl.  Scoring: a key is a pool row, numbered from the warp's first one
-    // (its rows' segments are consecutive pool rows).  The first batch's ancestry lookups are
-    // done here, before O arrives.
-    constexpr int kSlotBytes = 4 * D + 16;          // a key's K row, V row, one chunk of padding
-    constexpr int kSlots = kArea / kSlotBytes;      // keys staged at a time
-    static_assert(32 * (2 * D + 16) <= kArea, "the output rows pass through the area");
-    const int L = st.n_levels;
-    const int row_off = U.row_off;
-    const int nbw = G >= 32 ? 1 : 32 / G;           // beams the warp's rows belong to
-    const int bl = G >= 32 ? 0 : lane / G;          // this row's beam among them
-    auto key_row = [&](int j, int pool) -> int64_t {
-        return kScore ? ((int64_t)layer * st.rows + pool) * st.n_kv_heads + U.head
-                      : (((int64_t)layer * (L - 1) + j) * st.rows + pool) * st.n_kv_heads + U.head;
-    };
-    int lo = 0, total = 0;
-    auto key_of = [&](int p0) -> int64_t {  // the key lane l stages in batch p0 (-1: none)
-        const int idx = p0 + lane;
-        if (lane >= kSlots || idx >= total) return -1;
-        if constexpr (kScore) {
-            return key_row(0, lo + idx);
-        } else {
-            const int t = st.req_step[U.req];
-            const int j = idx / nbw, b = b_first + (idx - j * nbw);
-            if (b >= U.width || b >= st.n_beams[U.req * (L + 1) + t]) return -1;
-            return key_row(j, row_off + __ldg(st.path + ((int64_t)(t - 1) * st.rows + row_off + b) * L + j));
-        }
-    };
-    int64_t key0 = -1;
-    if (merger) {
-        if constexpr (kScore) {
-            lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(ri.live ? ri.pool0 : 0x7fffffff));
-            const int hi = __reduce_max_sync(0xffffffffu, ri.live ? ri.pool0 + ri.n_priv - 1 : -1);
-            total = hi >= lo ? hi - lo + 1 : 0;
-        } else {
-            total = __reduce_max_sync(0xffffffffu, ri.n_priv) * nbw;
-        }
-        key0 = key_of(0);
-    }
     uint32_t ov[D];  // this piece's unnormalised O row
-    if (!wait_o(ov)) return false;
+    if (!wait_o(ov)) return give_up();
     if (!merger) {
         // a later key range of a split unit: publish the normalised piece and its log-sum-exp;
         // the ready flag follows (see pend_flag).  The merger clears the flag once it has read
@@ -478,17 +539,44 @@ __device__ __forceinline__ bool job_epilogue(const GrState& st, const GrAttnUnit
     }
     // The first key range merges, by a log-sum-exp combine: its own O (registers), the other
     // pieces (finished earlier, at the start of their CTAs' ranges) and the beam part -- the
-    // row's private keys, folded in one key at a time with an online max.  Each warp copies the
-    // private keys' K and V rows of its 32 rows into its staging area (bulk copies, kSlots
-    // keys at a time), reads q from the job's Q tile, and finally passes its bf16 output rows
-    // through the same space, one bulk store per row.
+    // row's private keys, folded in one key at a time with an online max, from the staging
+    // area; q comes from the job's Q tile.
     float* a = reinterpret_cast<float*>(ov);  // the row accumulates in place of O
     {
         const float c_own = ri.live ? w_own * inv_l : 0.f;
 #pragma unroll
         for (int c = 0; c < D; ++c) a[c] = ri.live ? __uint_as_float(ov[c]) * c_own : 0.f;
     }
-    // ---- the beam part's set-up: the row's private keys are folded in one at a time
+    // ---- the published pieces
+#pragma unroll 1
+    for (int pp = 1; ri.live && pp <= n_other; ++pp) {
+        float w = 0.f;
+#pragma unroll
+        for (int k = 0; k < kPieceRegs; ++k) w = (k == pp - 1) ? wp[k] : w;
+        if (pp > kPieceRegs) {
+            w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
+            den += w;
+        }
+        const float4* src =
+            reinterpret_cast<const float4*>(st.o_part) + (int64_t)(U.first_slot + pp) * (D / 4) * kUnitRows + prow;
+        constexpr int kBatch = D / 8;  // chunks per batch of loads
+#pragma unroll
+        for (int c0 = 0; c0 < D / 4; c0 += kBatch) {
+            float4 x[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) x[u] = __ldcg(src + (int64_t)(c0 + u) * kUnitRows);
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                float* ac = a + 4 * (c0 + u);
+                ac[0] = fmaf(w, x[u].x, ac[0]);
+                ac[1] = fmaf(w, x[u].y, ac[1]);
+                ac[2] = fmaf(w, x[u].z, ac[2]);
+                ac[3] = fmaf(w, x[u].w, ac[3]);
+            }
+        }
+        st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
+    }
+    // ---- the beam part, one key at a time
     constexpr int kKC = D / 8;  // 16-byte chunks of a bf16 row
     // fold one key (its K and V rows) into (M, den, a)
     auto fold = [&](const uint4* kp, const uint4* vp) {
@@ -525,91 +613,52 @@ __device__ __forceinline__ bool job_epilogue(const GrState& st, const GrAttnUnit
             }
         }
     };
-    const uint32_t area_s = smem_u32(area);
-    auto copy = [&](int64_t key) {  // lane l stages one key (or none: key < 0) in slot l
-        const unsigned copies = __ballot_sync(0xffffffffu, key >= 0);
-        if (lane == 0) mbar_expect_tx(bbar, (uint32_t)__popc(copies) * (uint32_t)(4 * D));
-        __syncwarp();
-        if (key >= 0) {
-            bulk_load(area_s + lane * kSlotBytes, st.beam_k + key * D, 2 * D, bbar);
-            bulk_load(area_s + lane * kSlotBytes + 2 * D, st.beam_v + key * D, 2 * D, bbar);
-        }
-    };
-    // The staging area is free once the job's last key tile's MMAs have completed (no more
-    // tiles are loaded until merged() runs).  The first batch of copies goes out before the
-    // pieces are read, so that the two overlap.
-    if (!wait_area()) return false;
-    if (total > 0) copy(key0);
-    // ---- the published pieces
 #pragma unroll 1
-    for (int pp = 1; ri.live && pp <= n_other; ++pp) {
-        float w = 0.f;
-#pragma unroll
-        for (int k = 0; k < kPieceRegs; ++k) w = (k == pp - 1) ? wp[k] : w;
-        if (pp > kPieceRegs) {
-            w = __expf(__ldcg(lse_col + (int64_t)pp * kUnitRows) - M);
-            den += w;
-        }
-        const float4* src =
-            reinterpret_cast<const float4*>(st.o_part) + (int64_t)(U.first_slot + pp) * (D / 4) * kUnitRows + prow;
-        constexpr int kBatch = D / 8;  // chunks per batch of loads
-#pragma unroll
-        for (int c0 = 0; c0 < D / 4; c0 += kBatch) {
-            float4 x[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) x[u] = __ldcg(src + (int64_t)(c0 + u) * kUnitRows);
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                float* ac = a + 4 * (c0 + u);
-                ac[0] = fmaf(w, x[u].x, ac[0]);
-                ac[1] = fmaf(w, x[u].y, ac[1]);
-                ac[2] = fmaf(w, x[u].z, ac[2]);
-                ac[3] = fmaf(w, x[u].w, ac[3]);
-            }
-        }
-        st.piece_flag[(int64_t)(U.first_slot + pp) * kUnitRows + prow] = 0u;  // consumed
-    }
-    // ---- the beam part, one key at a time
-#pragma unroll 1
-    for (int p0 = 0; p0 < total; p0 += kSlots) {
-        if (p0 > 0) copy(key_of(p0));
-        const uint32_t par = bcnt & 1;
-        ++bcnt;
-        if (!wait_warp(bbar, par, wt)) {
-            wait_drain(bbar, par);  // no copy may land after the CTA has gone
-            return false;
-        }
+    for (int p0 = 0; p0 < ek.total; p0 += kSlots) {
+        if (p0 > 0) stage(p0 == kSlots ? ek.key1 : epi_key_row<kScore>(st, U, layer, ek.lo, ek.total, b_first, G, lane, p0));
+        cp_async_wait_all();
+        __syncwarp();  // every lane's copies have landed
         for (int j = 0; j < ri.n_priv; ++j) {
-            const int kidx = kScore ? ri.pool0 + j - lo : j * nbw + bl;
+            const int kidx = kScore ? ri.pool0 + j - ek.lo : j * nbw + bl;
             if (kidx < p0 || kidx >= p0 + kSlots) continue;
             const uint8_t* sl = area + (kidx - p0) * kSlotBytes;
             fold(reinterpret_cast<const uint4*>(sl), reinterpret_cast<const uint4*>(sl + 2 * D));
         }
         __syncwarp();  // every row is done with these slots before they are refilled
     }
+    // ---- the bf16 output rows (rows beyond the request are another request's: not written);
+    // dead beams come out as exact zeros (none of their unwritten inputs is used).  The rows
+    // pass through the staging area (one padding chunk per row against bank conflicts) so that
+    // each store instruction writes whole rows: lanes 0..kCpr-1 one row, the next kCpr lanes
+    // the next, and so on.
+    const float inv_den = ri.live ? 1.f / den : 0.f;
+    constexpr int kRowStride = 2 * D + 16;
+    constexpr int kCpr = D / 8;             // 16-byte chunks per bf16 row
+    constexpr int kRowsPer = 32 / kCpr;     // rows per store instruction
     {
-        // dead beams come out as exact zeros: none of their (unwritten) inputs is used
-        const float inv_den = ri.live ? 1.f / den : 0.f;
-#pragma unroll
-        for (int c = 0; c < D; ++c) a[c] = ri.live ? a[c] * inv_den : 0.f;
-    }
-    // ---- bf16 output rows (rows beyond the request are another request's: not written)
-    constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per bf16 row
-    {
-        // each row through the warp's staging area (rows padded by one chunk against bank
-        // conflicts), then one bulk store per row
-        constexpr int kRowStride = 2 * D + 16;
         uint8_t* stg = area + lane * kRowStride;
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c)
+        for (int c = 0; c < kCpr; ++c)
             *reinterpret_cast<uint4*>(stg + c * 16) =
-                make_uint4(pack_bf16x2(a[8 * c], a[8 * c + 1]), pack_bf16x2(a[8 * c + 2], a[8 * c + 3]),
-                           pack_bf16x2(a[8 * c + 4], a[8 * c + 5]), pack_bf16x2(a[8 * c + 6], a[8 * c + 7]));
-        fence_proxy_async_smem();  // the row's generic writes, then the bulk copy reads them
-        if (ri.row_ok) bulk_store(out + ri.orow_idx * D, smem_u32(stg), 2 * D);
-        bulk_commit_and_wait_read();  // the shared rows have been read
+                make_uint4(pack_bf16x2(a[8 * c] * inv_den, a[8 * c + 1] * inv_den),
+                           pack_bf16x2(a[8 * c + 2] * inv_den, a[8 * c + 3] * inv_den),
+                           pack_bf16x2(a[8 * c + 4] * inv_den, a[8 * c + 5] * inv_den),
+                           pack_bf16x2(a[8 * c + 6] * inv_den, a[8 * c + 7] * inv_den));
+    }
+    const int64_t orow = ri.row_ok ? ri.orow_idx : -1;
+    __syncwarp();
+    {
+        const int sub = lane / kCpr, ch = lane % kCpr;
+#pragma unroll 4
+        for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
+            const int r = r0 + sub;
+            const int64_t o = __shfl_sync(0xffffffffu, orow, r);
+            const uint4 v = *reinterpret_cast<const uint4*>(area + r * kRowStride + ch * 16);
+            if (o >= 0) reinterpret_cast<uint4*>(out + o * D)[ch] = v;
+        }
     }
     __syncwarp();
+    // the staging area and the Q tile are no longer needed: the next job's loads may start
     merged();
     return true;
 }

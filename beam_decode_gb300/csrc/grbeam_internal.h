@@ -21,6 +21,7 @@ constexpr int kTileRows = 128;        // query rows per tensor-core tile (TMEM l
 constexpr int kTileKeys = 128;        // context keys per tile
 constexpr int kUnitRows = 256;        // query rows per attention unit (two tiles)
 constexpr int kLogitCluster = 4;      // CTAs sharing one logit row
+constexpr int kTmapsPerReq = 3;       // ContextKV tensor maps of a request: K, V, K in half tiles of 64 keys
 
 // status word bits (device)
 constexpr int kStatusNanKey = 1;      // a candidate key was NaN
@@ -100,11 +101,12 @@ struct GrState {
     uint32_t* key_range;// [n_req][2] (~lower, upper) bound of the step's candidate keys (top-K)
 
     // attention
-    CUtensorMap* tmaps; // [n_req][2] (K, V) of the ContextKV pool
+    CUtensorMap* tmaps; // [n_req][kTmapsPerReq] (K, V, K half tiles) of the ContextKV pool
     GrAttnJob* jobs;    // [n_jobs]
     int2* cta_jobs;     // [n_cta] job range of each CTA
     GrAttnUnit* units;  // [n_units]
-    int n_units, n_jobs, n_cta;
+    int n_units, n_jobs, n_cta;  // n_cta: CTAs, or CTA pairs when attn_pair
+    int attn_pair;      // the decode attention runs on CTA pairs (k_pair_attn)
     float* o_part;      // [n_jobs][D][kUnitRows] pieces of split units (later key ranges), column-major
     float* lse_part;    // [n_jobs][kUnitRows]
     uint32_t* piece_flag; // [n_jobs][kUnitRows] 1 = piece row published and not yet merged
@@ -140,6 +142,10 @@ cudaError_t launch_rank(const float* lp, int n_labels, const int32_t* cand_off, 
 cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes);
 cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q, uint16_t* out,
                             int64_t wait_limit_ns, cudaStream_t s);
+// ---- launchers (k_attn_pair.cu) ----
+cudaError_t pair_attn_smem_bytes(size_t* bytes);
+cudaError_t launch_pair_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q, uint16_t* out,
+                             int64_t wait_limit_ns, cudaStream_t s);
 cudaError_t launch_score_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q, uint16_t* out,
                               int64_t wait_limit_ns, cudaStream_t s);
 

@@ -70,9 +70,14 @@ struct Plan {
     static constexpr int kStages = 2;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + 2 * kQTile;
-    static constexpr int kVOff = kKOff + kStages * kKVTile;
-    static constexpr int kBarOff = kVOff + kStages * kKVTile;
+    // the epilogue stages in the rings: query tile 0's four warps in the K ring and the pad
+    // after it, tile 1's in the V ring and the pad after that
+    static constexpr int kEpiArea = EpiArea<D>::kBytes;  // each softmax warp's staging space
+    static constexpr int kEpiPad = 4 * kEpiArea - kStages * kKVTile;
+    static constexpr int kVOff = kKOff + kStages * kKVTile + kEpiPad;
+    static constexpr int kBarOff = kVOff + kStages * kKVTile + kEpiPad;
     static constexpr int kBytes = kBarOff + 512 + 1024;  // barriers, TMEM address, abort flag, alignment
+    static_assert(kEpiPad >= 0 && kEpiPad % 1024 == 0, "the V ring stays 1024-byte aligned");
     // TMEM columns
     static constexpr int kTmemCols = 512;
     static __device__ __forceinline__ int s_col(int i) { return i * 128; }
@@ -83,9 +88,8 @@ struct Plan {
 enum Bar {
     B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2, B_K_EMPTY = 4, B_V_FULL = 6, B_V_EMPTY = 8,
     B_S_FULL = 10, B_P_FULL = 12, B_O_FULL = 14, B_O_EMPTY = 16, B_DRAIN = 18, B_PVD = 20,
-    B_BEAM = 22,  // one per softmax warp: its BeamKV rows copied into the freed rings
-    B_MERGED = 30,  // a merging job that is not the CTA's last has finished with the rings and Q
-    B_COUNT = 31
+    B_MERGED = 22,  // a merging job that is not the CTA's last has finished with the rings and Q
+    B_COUNT = 23
 };
 
 constexpr int kAttnThreads = 384;
@@ -123,7 +127,6 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             mbar_init(bar(B_DRAIN + k), 1);
             mbar_init(bar(B_PVD + k), 1);
         }
-        for (int k = 0; k < 8; ++k) mbar_init(bar(B_BEAM + k), 1);
         mbar_init(bar(B_MERGED), 8);  // one arrival per softmax warp (see the merge's end)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -153,7 +156,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 const GrAttnJob J = st.jobs[jb];
                 const GrAttnUnit& U = J.u;
                 if (!decoding<kScore>(st, U)) continue;
-                const CUtensorMap* km = st.tmaps + 2 * U.req;
+                const CUtensorMap* km = st.tmaps + kTmapsPerReq * U.req;
                 const CUtensorMap* vm = km + 1;
                 if (jb == jr.x || st.jobs[jb - 1].unit != J.unit) {
                     tmap_acquire(km);
@@ -308,7 +311,7 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
         const int row_t = quarter * 32 + lane;   // row within the tile
         const int prow = i * kTileRows + row_t;  // row within the unit
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        uint32_t tiles = 0, jobs = 0, ktiles = 0, bcnt = 0;
+        uint32_t tiles = 0, jobs = 0, ktiles = 0;
         bool ok = true;
         // A published piece's ready flag is raised once the next job's first key tile is done
         // (or when a job skips this warpgroup, or at the end): by then the piece's stores have
@@ -333,8 +336,9 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 continue;
             }
             const RowInfo ri = row_info<kScore>(st, U, i, row_t, G);
+            const int b_first = U.beam0 + i * (kTileRows / G) + (quarter * 32) / G;
+            const EpiKeys ek = epi_keys<D, kScore>(st, U, J, ri, layer, b_first, G, lane);  // looked up now
             const int ctx_len = U.ctx_len;
-            const bool merger = (J.slot == U.first_slot);
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int jj = 0; jj < n; ++jj) {
                 if (!(ok = wait_warp(bar(B_S_FULL + i), tiles & 1, wt))) break;
@@ -406,13 +410,10 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 raise_flag();
             }
             if (!ok) break;
-            const int b_first = U.beam0 + i * (kTileRows / G) + (quarter * 32) / G;
             const uint8_t* qs = smem + P::kQOff + i * P::kQTile + row_t * 128;  // this row in the Q tile
-            constexpr int kArea = P::kKVTile / 2;  // each softmax warp's share of the two rings
-            uint8_t* area = smem + P::kKOff + (warp - 4) * kArea;
-            ok = job_epilogue<D, kScore, kArea>(
-                st, U, J, ri, prow, row_t, lane, b_first, layer, scale, m_used, l, qs, area, bar(B_BEAM + warp - 4),
-                bcnt, pend_flag, out, wt,
+            uint8_t* area = smem + P::kKOff + (warp - 4) * P::kEpiArea;
+            ok = job_epilogue<D, kScore>(
+                st, U, J, ri, ek, row_t, lane, b_first, prow, layer, scale, m_used, l, qs, area, pend_flag, out, wt,
                 [&](uint32_t* ov) {
                     if (!wait_warp(bar(B_O_FULL + i), jobs & 1, wt)) return false;
                     tc_fence_after();

@@ -53,17 +53,17 @@ def _peaks():
 
 
 # DRAM bytes (read + write) per launch of the attention kernel from one ncu capture, keyed
-# by the sha256 of the kernel source it was taken on: (bytes per launch per request, note).
-# A kernel source without an entry reports traffic null.
-_ATTN_TRAFFIC = {
-    "4f10361a3bd242c5": (99.6e6 / 4, "ncu capture of the 4-request case, scaled by the number of requests"),
-}
+# by the sha256 of the kernel's sources it was taken on (the kernel file and the shared device
+# code): (bytes per launch per request, note).  Sources without an entry report traffic null.
+_ATTN_TRAFFIC = {}
 
 
 def _attn_traffic(w):
     import hashlib
-    src = os.path.join(ROOT, "beam_decode_gb300", "csrc", "k_attn.cu")
-    key = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in ("k_attn.cu", "attn_dev.cuh"):
+        h.update(open(os.path.join(ROOT, "beam_decode_gb300", "csrc", f), "rb").read())
+    key = h.hexdigest()[:16]
     if key not in _ATTN_TRAFFIC or w.name != "long" or len(set(w.ctx_lens)) != 1:
         return None
     per_req, _ = _ATTN_TRAFFIC[key]

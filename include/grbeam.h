@@ -152,15 +152,20 @@ gr_status gr_beam_kv_bytes(const gr_config* cfg, const gr_request* reqs, int n_r
 
 /* The attention schedule gr_beam_create builds for requests of these context
  * lengths (ctx_len[r] >= 1) and beam widths (beam_width[r] in 1..1024) on a
- * GPU with n_sm SMs.  Host only: no device, no trie, nothing allocated.
- * Only the head counts of cfg are read.  The decode attention kernel works
- * through this table, so it is the place to check its invariants without a
- * GPU.
+ * GPU with n_sm SMs, for the decode-attention kernel attn_kernel (0 the
+ * automatic choice, which is the single-CTA kernel; 1 the single-CTA kernel;
+ * 2 the CTA-pair kernel, head_dim 128 only; see gr_beam_set_attn_kernel).
+ * Host only: no device, no trie, nothing allocated.  Only the head counts and
+ * head_dim of cfg are read.  The decode attention kernel works through this
+ * table, so it is the place to check its invariants without a GPU.
  *
  * A unit is up to 256 query rows (two 128-row tiles) of one (request, KV
  * head).  Its key tiles of 128 keys are cut into contiguous ranges, the jobs,
  * spread over CTAs in order.  A unit's jobs own the consecutive piece slots
- * [first slot, first slot + slots); the job of the first range merges.
+ * [first slot, first slot + slots); the job of the first range merges.  For
+ * the CTA-pair kernel (each pair of CTAs computes a whole 256-row unit, one
+ * 128-row tile per CTA) the schedule is over n_sm / 2 pairs and "ctas" below
+ * are pairs.
  *   units [max_units][7] int32: request, KV head, first beam, query tiles,
  *                               first slot, slots, key tiles
  *   jobs  [max_jobs][4]  int32: unit, first key tile, end key tile, slot
@@ -168,11 +173,12 @@ gr_status gr_beam_kv_bytes(const gr_config* cfg, const gr_request* reqs, int n_r
  * *n_units, *n_jobs and *n_ctas are always written.  The arrays (caller-owned
  * host memory) are filled only when all three are large enough; otherwise
  * GR_ERR_CAPACITY is returned.  Errors: GR_ERR_INVALID_ARG (NULL pointer,
- * n_requests < 1, n_sm < 1, bad lengths or widths), GR_ERR_UNSUPPORTED
- * (query heads per KV head not 1, 2, 4, 8 or 16). */
+ * n_requests < 1, n_sm < 1, attn_kernel outside 0..2, bad lengths or widths),
+ * GR_ERR_UNSUPPORTED (query heads per KV head not 1, 2, 4, 8 or 16; the pair
+ * kernel with head_dim other than 128). */
 gr_status gr_attn_schedule(const gr_config* cfg, const int* ctx_len, const int* beam_width,
-                           int n_requests, int n_sm, int* n_units, int* n_jobs, int* n_ctas,
-                           int32_t* units, int max_units, int32_t* jobs, int max_jobs,
+                           int n_requests, int n_sm, int attn_kernel, int* n_units, int* n_jobs,
+                           int* n_ctas, int32_t* units, int max_units, int32_t* jobs, int max_jobs,
                            int32_t* ctas, int max_ctas);
 
 /* Validate the batch, carve the workspace, upload the request table, the
@@ -385,6 +391,17 @@ gr_status gr_beam_kernel_stats(gr_beam* beam, int kind, int64_t* launches, doubl
  * returns; the CUDA context stays usable.  A negative value makes every
  * pipeline wait give up on its first check, for fault-path tests. */
 gr_status gr_beam_set_wait_limit(gr_beam* beam, int64_t nanoseconds);
+
+/* Test hook: which decode-attention kernel the batch runs (between steps, not
+ * in graph mode): 0 the automatic choice (the single-CTA kernel), 1 the
+ * single-CTA kernel (two 128-row query tiles per CTA sharing whole K/V
+ * tiles), 2 the CTA-pair kernel (cta_group::2 MMAs, each CTA holding half of
+ * every K/V tile; head_dim 128 only, GR_ERR_UNSUPPORTED otherwise).  Both
+ * compute the same attention.  The schedule is rebuilt and its tables copied
+ * into the workspace on `stream`. */
+gr_status gr_beam_set_attn_kernel(gr_beam* beam, int mode, gr_stream_t stream);
+/* *pair = 1 when the batch runs the CTA-pair kernel, 0 for the single-CTA one. */
+gr_status gr_beam_attn_kernel(const gr_beam* beam, int* pair);
 
 /* ------------------------------------------------------------------------ */
 /* Constrained top-K without caller-provided scratch                         */

@@ -38,14 +38,20 @@ def expected_units(G, n_kv, ctx_lens, widths):
     return out
 
 
-def check_schedule(G, n_kv, ctx_lens, widths, n_sm):
-    units, jobs, ctas = B.attn_schedule(G * n_kv, n_kv, ctx_lens, widths, n_sm)
+def check_schedule(G, n_kv, ctx_lens, widths, n_sm, attn_kernel=0):
+    """attn_kernel 0 (automatic) and 1: the single-CTA kernel's schedule (one entry per CTA);
+    2: the CTA-pair kernel's, over n_sm / 2 pairs."""
+    units, jobs, ctas = B.attn_schedule(G * n_kv, n_kv, ctx_lens, widths, n_sm, head_dim=128,
+                                        attn_kernel=attn_kernel)
     exp = expected_units(G, n_kv, ctx_lens, widths)
     assert len(units) == len(exp)
     for u, e in zip(units, exp):
         assert (u[0], u[1], u[2], u[3], u[6]) == e
     tiles_all = sum(e[4] for e in exp)
-    assert len(ctas) == min(n_sm, tiles_all)
+    if attn_kernel == 2:
+        assert len(ctas) == min(max(n_sm // 2, 1), tiles_all)
+    else:
+        assert len(ctas) == min(n_sm, tiles_all)
     # CTA ranges partition the job list in order
     assert ctas[0, 0] == 0 and ctas[-1, 1] == len(jobs)
     assert np.all(ctas[1:, 0] == ctas[:-1, 1]) and np.all(ctas[:, 1] >= ctas[:, 0])
@@ -87,6 +93,7 @@ def test_schedule_invariants_random_batches(G, n_kv):
         widths = rng.choice(width_choices, size=n_req).astype(int)
         n_sm = int(rng.choice([1, 2, 7, 76, 148, 152]))
         check_schedule(G, n_kv, list(ctx), list(widths), n_sm)
+        check_schedule(G, n_kv, list(ctx), list(widths), n_sm, attn_kernel=2)
 
 
 def test_schedule_of_the_long_workload():
@@ -98,6 +105,22 @@ def test_schedule_of_the_long_workload():
     assert len(ctas) == 152
     # a CTA runs at most two jobs here: a piece of one unit, then the merger of the next
     assert np.max(ctas[:, 1] - ctas[:, 0]) <= 2
+    # the CTA-pair kernel: the same units over 76 CTA pairs
+    units, jobs, ctas = check_schedule(2, 8, [5000] * 8, [256] * 8, 152, attn_kernel=2)
+    assert len(ctas) == 76
+
+
+def test_kernel_choice_and_pair_kernel_limits():
+    """The automatic choice is the single-CTA kernel; the pair kernel needs head_dim 128."""
+    _, _, c0 = B.attn_schedule(16, 8, [5000] * 8, [256] * 8, 152, head_dim=128, attn_kernel=0)
+    _, _, c1 = B.attn_schedule(16, 8, [5000] * 8, [256] * 8, 152, head_dim=128, attn_kernel=1)
+    assert len(c0) == len(c1) == 152
+    with pytest.raises(B.GrError) as e:
+        B.attn_schedule(16, 8, [5000] * 8, [256] * 8, 152, head_dim=64, attn_kernel=2)
+    assert e.value.status == B.GR_ERR_UNSUPPORTED
+    with pytest.raises(B.GrError) as e:
+        B.attn_schedule(16, 8, [5000] * 8, [256] * 8, 152, attn_kernel=3)
+    assert e.value.status == B.GR_ERR_INVALID_ARG
 
 
 def test_schedule_degenerate_batches():
