@@ -55,7 +55,10 @@ def _peaks():
 # DRAM bytes (read + write) per launch of the attention kernel from one ncu capture, keyed
 # by the sha256 of the kernel's sources it was taken on (the kernel file and the shared device
 # code): (bytes per launch per request, note).  Sources without an entry report traffic null.
-_ATTN_TRAFFIC = {}
+_ATTN_TRAFFIC = {
+    "a0f08e9ecee0110a": ((222.06e6 + 4.29e6) / 8,
+                         "ncu capture of one launch at the long shapes (8 requests, one layer), per request"),
+}
 
 
 def _attn_traffic(w):
@@ -129,6 +132,25 @@ class DeviceBatch:
             b.decode_attn(l, self.q[l], self.out[l])
         b.constrained_topk(self.logits[1])
         b.advance()
+
+    def finish(self):
+        """Decode the batch on to its last levels from the state a step leaves (the level just
+        selected has no BeamKV yet): each further step writes that level's BeamKV, then runs
+        attention, top-K and advance, until every request has reached its last level."""
+        b, w = self.beam, self.w
+
+        def unfinished():
+            return any(t < L for t, L in (b.request_step(r) for r in range(w.n_requests)))
+
+        while unfinished():
+            for l in range(w.n_layers):
+                k, v = b.kv_slot(l)
+                k.copy_(self.new_k[l])
+                v.copy_(self.new_v[l])
+            for l in range(w.n_layers):
+                b.decode_attn(l, self.q[l], self.out[l])
+            b.constrained_topk(self.logits[1])
+            b.advance()
 
     def capture(self):
         """Record the step once as a CUDA graph (graph mode: every decision inside comes from
@@ -229,8 +251,8 @@ def oracle_step_seconds(w: wl.Workload, budget_s: float = 12.0):
         beam_attention(q, ck, cv, bk, bv, anc, beams=[n_att])
         n_att += 1
     att_s = (time.perf_counter() - t0) / n_att  # one (beam, layer): all q heads
-    # top-K of one request at step 1 (full width)
-    items = wl.draw_items(min(w.n_items[0], 200_000), w.n_levels, w.codes_per_level, w.trie_dist, w.seed)
+    # top-K of one request at step 1 (full width) over the workload's whole catalogue
+    items = wl.draw_items(w.n_items[0], w.n_levels, w.codes_per_level, w.trie_dist, w.seed)
     trie = Trie(items, codes_per_level=w.codes_per_level)
     ob = OracleBeam(trie, W, w.n_levels, w.codes_per_level, w.code_base)
     x0 = wl.host_normal((1, w.vocab), rng_seed, wl.TAG_LOGITS, std=w.logit_std)
@@ -243,7 +265,8 @@ def oracle_step_seconds(w: wl.Workload, budget_s: float = 12.0):
     per_step = (att_s * W * w.n_layers + topk_s) * w.n_requests
     sample = (f"oracle on request 0: naive float64 attention of {n_att} beams x {w.n_q_heads} heads at one layer "
               f"({att_s * 1e3:.1f} ms per beam-layer) scaled x{W} beams x{w.n_layers} layers x{w.n_requests} "
-              f"requests; constrained top-K of {n1} live rows ({topk_s:.2f} s) x{w.n_requests} requests")
+              f"requests; constrained top-K of {n1} live rows over {w.n_items[0]} items ({topk_s:.2f} s) "
+              f"x{w.n_requests} requests")
     return per_step, sample
 
 
@@ -404,6 +427,15 @@ def run_gpu(args, w):
         ms, ck = timed(batch.graph.replay, True)
         launches = per_step * args.steps
         batch.release()
+    # k_results runs once a decode is finished: decode the batch on to its last level and
+    # time one results call per request (outside the timed step)
+    batch.finish()
+    beam.set_timing(True)
+    for r in range(w.n_requests):
+        beam.results(r)
+    beam.set_timing(False)
+    stats["results"] = beam.kernel_stats(B.KERNEL_NAMES.index("results"), reset=True)
+    batch.step()  # back to the state a timed step leaves (level 1 selected)
     ms_per_step = ms / args.steps
     value = job_value(ms_per_step, world)
     st = beam.status()
@@ -425,17 +457,12 @@ def run_gpu(args, w):
                 "peak_kind": f"{pk['src']} burst bf16"}
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, batch) if rank == 0 else None
+    e2e = run_e2e(args, batch) if (rank == 0 and not args.no_e2e) else None
     scoring = run_scoring(args, dev) if (rank == 0 and not args.no_scoring) else None
 
     per_kernel = {k: {"launches": n, "ms_per_launch": (t / n if n else 0.0), "ms_per_step": t / args.steps}
                   for k, (n, t) in stats.items() if n}
-    hbm = {}
-    n, t = stats["logsoftmax_gather"]
-    if n:
-        byts = batch.rows * w.vocab * 4.0
-        hbm["logsoftmax_gather"] = {"GB_s": byts / (t / n * 1e-3) / 1e9,
-                                    "frac": byts / (t / n * 1e-3) / 1e9 / pk["hbm"]}
+    hbm = small_kernel_hbm(batch, stats, pk)
 
     if rank == 0:
         cpu_s, sample = oracle_step_seconds(w, budget_s=12.0) if not args.no_cpu else (float("nan"), "skipped")
@@ -533,6 +560,37 @@ def run_scoring(args, device):
             "labels_ms": ms - att_ms}
 
 
+def small_kernel_hbm(batch, stats, pk):
+    """Algorithmic HBM bytes / CUDA-event time per launch of the step's memory-bound kernels
+    (the step is t = 1 at full width: n_live = W_r beams per request).  logsoftmax_gather
+    reads every live row's fp32 logits once.  topk_select reads the C candidate keys of every
+    live beam and writes W_r (parent, code, key) triples per request.  advance reads a beam's
+    selection (parent, code, key), its parent's trie node, the node's child base and on
+    average C/64 + 1 mask words below its code, and its parent's ancestry row (t entries);
+    it writes parent, token, node, score and the ancestry row (t + 1 entries).  results (one
+    launch per request, after the batch is decoded to its last level L) reads each final
+    beam's ancestry row, the L tokens it names, its node and leaf item and its score, and
+    writes L codes, the item id and the score.  The small kernels are bound by launch
+    latency, not bandwidth: their fractions say how far from the HBM roofline that leaves
+    them."""
+    w = batch.w
+    C, L = w.codes_per_level, w.n_levels
+    beams = float(sum(w.beam_widths))
+    per_launch = {
+        "logsoftmax_gather": batch.rows * w.vocab * 4.0,
+        "topk_select": beams * C * 4.0 + beams * 12.0,
+        "advance": beams * (12.0 + 4.0 + 4.0 + 4.0 * (C / 64 + 1) + 4.0 * 1 + 16.0 + 4.0 * 2),
+        "results": beams / w.n_requests * (8.0 * L + 4.0 + 8.0 + 4.0 + 4.0 * L + 8.0 + 4.0),
+    }
+    hbm = {}
+    for k, byts in per_launch.items():
+        n, t = stats.get(k, (0, 0.0))
+        if n:
+            gbs = byts / (t / n * 1e-3) / 1e9
+            hbm[k] = {"GB_s": gbs, "frac": gbs / pk["hbm"], "bytes_per_launch": byts, "us_per_launch": t / n * 1e3}
+    return hbm
+
+
 def run_e2e(args, batch: DeviceBatch):
     """Same step through the public API with pinned host inputs copied in and the
     step's selection read back every step.  The copies run on their own stream,
@@ -628,11 +686,16 @@ def main():
     ap.add_argument("--no-scoring", action="store_true", help="skip the multi-item scoring measurement")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests of the workload (a smaller case for profiling)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="keep only the first N layers (a smaller case for profiling: same per-launch shapes)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     args = ap.parse_args()
     w = wl.make_workload(args.workload)
     if args.requests:
         n = args.requests
         w.ctx_lens, w.beam_widths, w.n_items = w.ctx_lens[:n], w.beam_widths[:n], w.n_items[:n]
+    if args.layers:
+        w.n_layers = min(args.layers, w.n_layers)
     if args.impl == "reference":
         return run_reference(args, w)
     from beam_decode_gb300.build import build

@@ -215,18 +215,24 @@ gr_status gr_beam_kv_slot_request(gr_beam* beam, int layer, int request, void** 
 /* GQA decode attention, layer `layer`, of every live beam of every request at
  * a step 1 <= t_r < L_r: beam b of request r attends to its request's T_r
  * context tokens followed by the t_r BeamKV tokens on its path (levels
- * 0..t_r-1, slots from BeamPath), scale 1/sqrt(D).
+ * 0..t_r-1, slots from BeamPath), scale 1/sqrt(D).  This is the attention
+ * backend that works directly on the ContextKV / BeamKV / BeamPath layout
+ * (gr-decode_atten in the zhiding.cn recsys-examples article, section
+ * "语义ID生成式推荐专用推理框架").
  *   q   bf16 [rows][n_q_heads][head_dim], 16-byte aligned
  *   out bf16 [rows][n_q_heads][head_dim]; rows of dead beams of those requests
  *       are written as zeros, rows of other requests (t_r == 0 or finished)
  *       are not written
- * The context part runs on the tensor cores (tcgen05, TMA-fed, every context
- * byte read once per request), the BeamKV part with vector loads, merged by
- * a log-sum-exp combine.  Each layer may be called once per step. */
+ * The context part runs on the tensor cores (tcgen05, TMA-fed), the BeamKV
+ * part from rows staged in shared memory by asynchronous copies, merged by a
+ * log-sum-exp combine.  Each layer may be called once per step. */
 gr_status gr_decode_attn(gr_beam* beam, int layer, const void* q, void* out, gr_stream_t stream);
 
 /* Full-vocabulary log-softmax of every live row, then the item-constrained
- * top-K of each request across (beam, code) candidates of level t:
+ * top-K of each request across (beam, code) candidates of level t (the beam
+ * scores come from the output logits: same article, section
+ * "语义ID：解决稀疏性与长尾问题"; the item-constrained top-K and the dynamic
+ * beam width: section "语义ID生成式推荐专用推理框架"):
  *   key(b, c) = S_b + (x[b][code_base + t*C + c] - LSE_b)   (float32, each
  *   operation rounded once), over codes c valid after beam b's prefix;
  *   order: key descending, then flat index b*C + c ascending;
@@ -244,7 +250,10 @@ gr_status gr_constrained_topk(gr_beam* beam, const float* logits, int64_t ld, fl
 
 /* Commit each decoding request's selection of its step t_r to BeamPath
  * (parent slot, token, trie node, score, ancestry) and set the live width of
- * step t_r+1; no KV is moved.  Every decoding request moves to t_r+1. */
+ * step t_r+1; no KV is moved: beams are tracked through their ancestry
+ * instead of being kept as independent long sequences (BeamPath, same
+ * article, section "语义ID生成式推荐专用推理框架").  Every decoding request
+ * moves to t_r+1. */
 gr_status gr_beam_advance(gr_beam* beam, gr_stream_t stream);
 
 /* Every request past step `step` goes back to it, so that it can be decoded
@@ -275,7 +284,11 @@ gr_status gr_beam_set_graph_mode(gr_beam* beam, int enable);
 gr_status gr_beam_sync(gr_beam* beam, gr_stream_t stream);
 
 /* All surviving beams of request `request` once it finished (t_r == L_r),
- * best first (synchronises `stream`):
+ * best first (beam search returns every surviving beam, not only the best:
+ * "Advancing Generative Recommendation Inference: our collaboration with
+ * NVIDIA on TensorRT LLM", section "Background: what inference a
+ * recommendation request needs"); synchronises `stream`.  A beam's parents
+ * at every level are read with gr_beam_path.
  *   codes     int32 [W_r][L_r]        code of each level
  *   item_ids  int64 [W_r]             item of the code string
  *   scores    fp32  [W_r]             sum of the code log-probabilities
@@ -428,17 +441,18 @@ gr_status gr_beam_attn_kernel(const gr_beam* beam, int* pair);
  *   out_n        device int32 [1]: number written
  * Limits: n_rows * n_codes <= GR_NOALLOC_MAX_CANDIDATES, n_codes <= 1024,
  * k <= 1024; larger sizes return GR_ERR_CAPACITY and launch nothing.
- * Scratch: the candidate keys live in one fixed device array of the library
- * (GR_NOALLOC_MAX_CANDIDATES x 4 bytes = 1 MiB) that every GPU which loads
- * the library holds until the process exits.  The call allocates nothing:
- * no cudaMalloc, no cudaFree, no allocating library routine.  Every call on
- * a device shares that one array and overwrites it completely, so calls that
- * overlap on the GPU (concurrent streams, or several host threads) race and
- * must be serialised by the caller; calls queued on one stream are fine.
- * The first call on each device looks the array's device address up
- * (cudaGetSymbolAddress with that device current); make that first call
- * before any stream capture on that device.  Enqueues two kernels on
- * `stream` and returns without synchronising. */
+ * Scratch: the candidate keys and the candidates' key range live in one
+ * fixed device array of the library (GR_NOALLOC_MAX_CANDIDATES x 4 bytes =
+ * 1 MiB, plus 256 bytes) that every GPU which loads the library holds until
+ * the process exits.  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.  The key range must start at
+ * zero: it does when the library is loaded, and every call's last kernel
+ * clears it again.  Every call on a device shares that one array and
+ * overwrites it, so calls that overlap on the GPU (concurrent streams, or
+ * several host threads) race and must be serialised by the caller; calls
+ * queued on one stream are fine.  Each call looks the array's device address
+ * up (cudaGetSymbolAddress, with the current device).  Enqueues two kernels
+ * on `stream` and returns without synchronising. */
 #define GR_NOALLOC_MAX_CANDIDATES (256 * 1024)
 gr_status gr_constrained_topk_noalloc(const float* logits, int64_t ld, int n_rows, int vocab, int code_lo,
                                       int n_codes, const float* beam_scores, const uint32_t* valid_mask, int k,
