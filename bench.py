@@ -384,6 +384,8 @@ def run_gpu(args, w):
     dev = f"cuda:{local}"
     w = replica_workload(w, rank)
     batch = DeviceBatch(w, dev)
+    if args.attn_kernel != "auto":
+        batch.beam.set_attn_kernel({"single": 1, "pair": 2}[args.attn_kernel])
     beam = batch.beam
     stream = torch.cuda.current_stream()
 
@@ -479,7 +481,7 @@ def run_gpu(args, w):
                            "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "vocab": w.vocab,
                            "levels": w.n_levels, "codes": w.codes_per_level, "items": w.n_items[0],
                            "l2": "inputs larger than L2 (ContextKV %.2f GB)" % (batch.ctx_bytes_per_layer() * w.n_layers / 1e9), "parallelism": f"replicas{world}",
-                           "cuda_graph": not args.no_graph},
+                           "cuda_graph": not args.no_graph, "attn_kernel": beam.attn_kernel()},
                 "eager": {"value": job_value(ms_eager / args.steps, world), "unit": "steps/s",
                           "ms_per_step": ms_eager / args.steps},
                 "roofline": roofline,
@@ -568,11 +570,11 @@ def small_kernel_hbm(batch, stats, pk):
     selection (parent, code, key), its parent's trie node, the node's child base and on
     average C/64 + 1 mask words below its code, and its parent's ancestry row (t entries);
     it writes parent, token, node, score and the ancestry row (t + 1 entries).  results (one
-    launch per request, after the batch is decoded to its last level L) reads each final
-    beam's ancestry row, the L tokens it names, its node and leaf item and its score, and
-    writes L codes, the item id and the score.  The small kernels are bound by launch
-    latency, not bandwidth: their fractions say how far from the HBM roofline that leaves
-    them."""
+    launch per gr_beam_results call, after the batch is decoded to its last level L; each
+    launch covers every request) reads each final beam's ancestry row, the L tokens it
+    names, its node and leaf item and its score, and writes L codes, the item id and the
+    score.  The small kernels are bound by launch latency, not bandwidth: their fractions
+    say how far from the HBM roofline that leaves them."""
     w = batch.w
     C, L = w.codes_per_level, w.n_levels
     beams = float(sum(w.beam_widths))
@@ -580,7 +582,7 @@ def small_kernel_hbm(batch, stats, pk):
         "logsoftmax_gather": batch.rows * w.vocab * 4.0,
         "topk_select": beams * C * 4.0 + beams * 12.0,
         "advance": beams * (12.0 + 4.0 + 4.0 + 4.0 * (C / 64 + 1) + 4.0 * 1 + 16.0 + 4.0 * 2),
-        "results": beams / w.n_requests * (8.0 * L + 4.0 + 8.0 + 4.0 + 4.0 * L + 8.0 + 4.0),
+        "results": beams * (8.0 * L + 4.0 + 8.0 + 4.0 + 4.0 * L + 8.0 + 4.0),
     }
     hbm = {}
     for k, byts in per_launch.items():
@@ -689,6 +691,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers (a smaller case for profiling: same per-launch shapes)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--attn-kernel", default="auto", choices=["auto", "single", "pair"],
+                    help="decode-attention kernel (auto: the library's choice)")
     args = ap.parse_args()
     w = wl.make_workload(args.workload)
     if args.requests:
