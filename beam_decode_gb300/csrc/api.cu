@@ -631,6 +631,10 @@ gr_status build_tables(gr_beam* h) {
             return s;
     }
     h->st.attn_pair = pair ? 1 : 0;
+    // the single-CTA kernel double-buffers S when no unit has a second query tile
+    bool one = !pair;
+    for (const auto& u : h->sched.units) one = one && u.nqt == 1;
+    h->st.attn_one = one ? 1 : 0;
     finalize_jobs(h->sched, rq);
     memcpy(img + w.jobs, h->sched.jobs.data(), sizeof(GrAttnJob) * h->sched.jobs.size());
     memcpy(img + w.cta_jobs, h->sched.cta_jobs.data(), sizeof(int2) * h->sched.cta_jobs.size());

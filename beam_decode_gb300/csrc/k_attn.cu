@@ -94,7 +94,11 @@ enum Bar {
 
 constexpr int kAttnThreads = 384;
 
-template <int D, bool kScore>
+// kOne: every unit of the launch has a single query tile (at most 128 rows).  Query tile 1's
+// TMEM columns then serve as a second S buffer for tile 0: S^g goes to buffer g & 1, so S of
+// the next key tile is computed while the softmax of this one runs, and only S^(g+2) waits for
+// PV^g (which reads P^g from the same buffer).  Warps 8-11 have no rows and idle.
+template <int D, bool kScore, bool kOne = false>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, const uint16_t* __restrict__ q,
            uint16_t* __restrict__ out, float scale_log2, float scale, int64_t wait_limit_ns) {
@@ -218,9 +222,10 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                         const int ks = kit & 1;
                         if (!(ok = wait1(bar(B_K_FULL + ks), (kit >> 1) & 1, wt))) break;
                         for (int i = 0; i < nqt; ++i) {
-                            if (s_i[i] > 0 && !(ok = wait1(bar(B_PVD + i), (s_i[i] - 1) & 1, wt))) break;
+                            const int bi = kOne ? (int)(kit & 1) : i;  // the S buffer
+                            if (s_i[bi] > 0 && !(ok = wait1(bar(B_PVD + bi), (s_i[bi] - 1) & 1, wt))) break;
                             tc_fence_after();
-                            const uint32_t d = tmem + P::s_col(i);
+                            const uint32_t d = tmem + P::s_col(bi);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
                                 const uint32_t off = (kk >> 2) * P::kBoxBytes + (kk & 3) * 32;
@@ -229,8 +234,8 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                                 mma_ss(d, a, b, idesc_s, kk > 0 ? 1u : 0u);
                             }
                             mma_issued = true;
-                            tc_commit(bar(B_S_FULL + i));
-                            ++s_i[i];
+                            tc_commit(bar(B_S_FULL + bi));
+                            ++s_i[bi];
                         }
                         if (!ok) break;
                         tc_commit(bar(B_K_EMPTY + ks));
@@ -251,21 +256,22 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                         const int vs = vit & 1;
                         if (!(ok = wait1(bar(B_V_FULL + vs), (vit >> 1) & 1, wt))) break;
                         for (int i = 0; i < nqt; ++i) {
-                            if (!(ok = wait1(bar(B_P_FULL + i), pv_i[i] & 1, wt))) break;
+                            const int bi = kOne ? (int)(vit & 1) : i;  // the P buffer
+                            if (!(ok = wait1(bar(B_P_FULL + bi), pv_i[bi] & 1, wt))) break;
                             if (jj == 0 && jobs_i[i] > 0 && !(ok = wait1(bar(B_O_EMPTY + i), (jobs_i[i] - 1) & 1, wt)))
                                 break;
                             tc_fence_after();
                             const uint32_t d = tmem + P::o_col(i);
 #pragma unroll
                             for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-                                const uint32_t a = tmem + P::p_col(i) + kk * 8;
+                                const uint32_t a = tmem + P::p_col(bi) + kk * 8;
                                 const uint64_t b =
                                     smem_desc(sb + P::kVOff + vs * P::kKVTile + kk * 16 * 128, P::kBoxBytes, 1024);
                                 mma_ts(d, a, b, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
                             }
                             mma_issued = true;
-                            tc_commit(bar(B_PVD + i));  // S_i of the next tile may overwrite P_i
-                            ++pv_i[i];
+                            tc_commit(bar(B_PVD + bi));  // the next S of this buffer may overwrite P
+                            ++pv_i[bi];
                             if (jj == n - 1) tc_commit(bar(B_O_FULL + i));
                         }
                         if (!ok) break;
@@ -341,10 +347,11 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
             const int ctx_len = U.ctx_len;
             float m_used = -CUDART_INF_F, l = 0.f;
             for (int jj = 0; jj < n; ++jj) {
-                if (!(ok = wait_warp(bar(B_S_FULL + i), tiles & 1, wt))) break;
+                const int bs = kOne ? (int)(tiles & 1) : i;  // the S / P buffer of this key tile
+                if (!(ok = wait_warp(bar(B_S_FULL + bs), (kOne ? tiles >> 1 : tiles) & 1, wt))) break;
                 tc_fence_after();
                 uint32_t sv[128];
-                tmem_ld128(tmem + lane_base + P::s_col(i), sv);
+                tmem_ld128(tmem + lane_base + P::s_col(bs), sv);
                 const int valid = ctx_len - (J.t0 + jj) * kTileKeys;
                 if (valid < kTileKeys) {
 #pragma unroll
@@ -366,6 +373,11 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 } else {
                     const bool need = (mx - m_used) * scale_log2 > 8.f;
                     if (__any_sync(0xffffffffu, need)) {
+                        // O holds the previous key tiles once the last PV has completed (with one
+                        // S buffer per query tile this S waited for it; with kOne it did not)
+                        if (kOne && !(ok = wait_warp(bar(B_PVD + ((tiles - 1) & 1)), ((tiles - 1) >> 1) & 1, wt)))
+                            break;
+                        tc_fence_after();
                         const float m_new = need ? mx : m_used;
                         const float alpha = exp2f((m_used - m_new) * scale_log2);
 #pragma unroll 1
@@ -401,11 +413,11 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 f2_unpack(acc[2], s4, s5);
                 f2_unpack(acc[3], s6, s7);
                 l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-                tmem_st32(tmem + lane_base + P::p_col(i), sv);
-                tmem_st32(tmem + lane_base + P::p_col(i) + 32, sv + 32);
+                tmem_st32(tmem + lane_base + P::p_col(bs), sv);
+                tmem_st32(tmem + lane_base + P::p_col(bs) + 32, sv + 32);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(B_P_FULL + i));
+                mbar_arrive(bar(B_P_FULL + bs));
                 ++tiles;
                 raise_flag();
             }
@@ -456,12 +468,12 @@ cudaError_t ctx_attn_smem_bytes(int head_dim, size_t* bytes) {
     return cudaSuccess;
 }
 
-template <int D, bool kScore>
+template <int D, bool kScore, bool kOne>
 cudaError_t launch_ctx_attn_d(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,
                               uint16_t* out, float scale_log2, float scale, int64_t wait_limit_ns, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_ctx_attn<D, kScore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(k_ctx_attn<D, kScore, kOne>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Plan<D>::kBytes);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -478,7 +490,7 @@ cudaError_t launch_ctx_attn_d(const GrState& st, const CUtensorMap& qmap, int la
     at[0].val.cooperative = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_ctx_attn<D, kScore>, qmap, st, layer, q, out, scale_log2, scale,
+    return cudaLaunchKernelEx(&cfg, k_ctx_attn<D, kScore, kOne>, qmap, st, layer, q, out, scale_log2, scale,
                               wait_limit_ns);
 }
 
@@ -488,9 +500,14 @@ cudaError_t launch_attn(const GrState& st, const CUtensorMap& qmap, int layer, c
     const float scale = 1.f / sqrtf((float)st.head_dim);
     const float scale_log2 = scale * 1.4426950408889634f;
     if (st.head_dim != 128 && st.head_dim != 64) return cudaErrorInvalidValue;
+    if (!kScore && st.attn_one) {  // every unit one query tile wide: two S buffers for it
+        if (st.head_dim == 128)
+            return launch_ctx_attn_d<128, false, true>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
+        return launch_ctx_attn_d<64, false, true>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
+    }
     if (st.head_dim == 128)
-        return launch_ctx_attn_d<128, kScore>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
-    return launch_ctx_attn_d<64, kScore>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
+        return launch_ctx_attn_d<128, kScore, false>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
+    return launch_ctx_attn_d<64, kScore, false>(st, qmap, layer, q, out, scale_log2, scale, wait_limit_ns, s);
 }
 
 cudaError_t launch_ctx_attn(const GrState& st, const CUtensorMap& qmap, int layer, const uint16_t* q,

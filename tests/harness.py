@@ -39,6 +39,8 @@ class Spec:
     ld_pad: int = 0
     seed: int = 0
     pool_gap: int = 7      # unused tokens between requests in the ContextKV pool
+    q_std: float = 1.0     # queries ~ N(0, q_std^2): larger values make the running row max grow
+                           # across key tiles, which exercises the online-softmax rescale
 
     @staticmethod
     def from_workload(w: wl.Workload, **over) -> "Spec":
@@ -124,8 +126,8 @@ class LockStep:
 
     def queries(self, t: int, layer: int) -> np.ndarray:
         s = self.spec
-        return wl.round_to_bf16(wl.host_normal((self.beam.rows, s.n_q_heads, s.head_dim), s.seed, wl.TAG_Q,
-                                               sub=(t, layer)))
+        return wl.round_to_bf16(s.q_std * wl.host_normal((self.beam.rows, s.n_q_heads, s.head_dim), s.seed,
+                                                         wl.TAG_Q, sub=(t, layer)))
 
     # -- one attention layer -------------------------------------------------------
     def attention(self, layer: int, requests=None, beams_per_request=None) -> Dict:

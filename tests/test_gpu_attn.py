@@ -63,3 +63,15 @@ def test_layers_are_independent():
     for layer in [0, 2, 1, 3]:
         worst = max(worst, ls.attention(layer)["worst"])
     assert worst <= 1.0
+
+
+@pytest.mark.parametrize("q_std", [1.0, 8.0])
+def test_one_tile_units_two_s_buffers(q_std):
+    # every unit is one query tile (beam 30 x 2 query heads = 60 rows, as in the page1 workload),
+    # so the kernel double-buffers S; q_std 8 spreads the scores so that the running row max
+    # grows across key tiles and O is rescaled while the next tile's S is already computed
+    spec = Spec(n_layers=2, n_q_heads=4, n_kv_heads=2, head_dim=128, vocab=4096, n_levels=3,
+                codes_per_level=128, code_base=4096 - 384, ctx_lens=[2000, 129, 4097, 640],
+                widths=[30, 30, 30, 12], n_items=[5000] * 4, q_std=q_std, seed=91)
+    _, res = _run(spec, steps=2)
+    assert max(r["worst"] for r in res) <= 1.0, res
