@@ -75,3 +75,14 @@ def test_one_tile_units_two_s_buffers(q_std):
                 widths=[30, 30, 30, 12], n_items=[5000] * 4, q_std=q_std, seed=91)
     _, res = _run(spec, steps=2)
     assert max(r["worst"] for r in res) <= 1.0, res
+
+
+def test_one_tile_units_many_jobs_per_cta():
+    # 96 one-tile units of 12 key tiles over the CTAs: every CTA runs several jobs, so the
+    # epilogue warps finish one job (pieces published, merges with BeamKV keys at t = 1, 2)
+    # while the key-tile warps already run the next
+    spec = Spec(n_layers=1, n_q_heads=8, n_kv_heads=4, head_dim=128, vocab=4096, n_levels=3,
+                codes_per_level=128, code_base=4096 - 384, ctx_lens=[1500] * 20 + [300, 3000, 129, 1],
+                widths=[30] * 24, n_items=[4000] * 24, seed=93)
+    _, res = _run(spec, steps=2)
+    assert max(r["worst"] for r in res) <= 1.0, res
