@@ -354,7 +354,8 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     // ~83 ns): a key tile costs 20 with two query tiles (they ping-pong) and 17 with one;
     // every job after a CTA's first costs kSwitch more (publish, the next job's Q, pipeline
     // refill); a unit's first key range, the merger, costs kMerge more (pieces, BeamKV keys,
-    // output).  The makespan bound T is the smallest for which a greedy walk fits every
+    // output).  kMerge = 75 came from a sweep over the long, short, mixed and page1 workloads
+    // (75 against 105: page1 -3 %, mixed -1 %, the others unchanged).  The makespan bound T is the smallest for which a greedy walk fits every
     // unit into n_cta CTAs: units and key tiles in order (so the units of a KV head stay on
     // neighbouring CTAs), a unit cut where a CTA's budget runs out.  A cut unit's first range
     // is then the last job of its CTA and its later ranges are the first jobs of the next
@@ -362,7 +363,7 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     // The pair kernel (cost in the same units): a key tile costs a pair 7 with one or two
     // query tiles (each CTA computes its 128 rows of an M = 256 MMA), a job switch 30, a
     // merge 100.
-    const int64_t kSwitch = pair ? 30 : 36, kMerge = pair ? 100 : 105;
+    const int64_t kSwitch = pair ? 30 : 36, kMerge = pair ? 100 : 75;
     auto tile_cost = [pair](const GrAttnUnit& u) -> int64_t { return pair ? 7 : (u.nqt == 2 ? 20 : 17); };
     // returns the CTAs used (n_cta + 1: does not fit); with emit, writes jobs and ranges
     auto walk = [&](int64_t T, bool emit) -> int {
