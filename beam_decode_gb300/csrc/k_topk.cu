@@ -267,41 +267,49 @@ __global__ void __launch_bounds__(kRankThreads) k_rank(const float* __restrict__
     if (tid < n) rank_out[c0 + tid] = (int32_t)(0xFFFFFFFFu - (uint32_t)(e[tid] & 0xFFFFFFFFull));
 }
 
+// Launch status of this launch only (cudaLaunchKernelEx's return value): a pending error of
+// unrelated earlier work stays with the caller.  A kernel compiled with cluster dimensions keeps
+// them.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace
 
 cudaError_t launch_label_logprobs(const float* logits, int64_t ld, int vocab, const int32_t* labels, int n_labels,
                                   int n_rows, float* out, int32_t* status, cudaStream_t s) {
-    k_label_logprobs<<<n_rows * kLogitCluster, kLsThreads, 0, s>>>(logits, ld, vocab, labels, n_labels, out, status);
-    return cudaGetLastError();
+    return launch(k_label_logprobs, dim3(n_rows * kLogitCluster), dim3(kLsThreads), 0, s, logits, ld, vocab, labels,
+                  n_labels, out, status);
 }
 
 cudaError_t launch_rank(const float* lp, int n_labels, const int32_t* cand_off, int n_req, int32_t* rank_out,
                         int32_t* status, cudaStream_t s) {
-    k_rank<<<n_req, kRankThreads, 0, s>>>(lp, n_labels, cand_off, rank_out, status);
-    return cudaGetLastError();
+    return launch(k_rank, dim3(n_req), dim3(kRankThreads), 0, s, lp, n_labels, cand_off, rank_out, status);
 }
 
 cudaError_t launch_init_state(const GrState& st, cudaStream_t s) {
-    k_init_state<<<1, 256, 0, s>>>(st);
-    return cudaGetLastError();
+    return launch(k_init_state, dim3(1), dim3(256), 0, s, st);
 }
 
 cudaError_t launch_init_request(const GrState& st, int r, cudaStream_t s) {
-    k_init_request<<<1, 32, 0, s>>>(st, r);
-    return cudaGetLastError();
+    return launch(k_init_request, dim3(1), dim3(32), 0, s, st, r);
 }
 
 cudaError_t launch_set_step(const GrState& st, int step, cudaStream_t s) {
-    k_set_step<<<1, 256, 0, s>>>(st, step);
-    return cudaGetLastError();
+    return launch(k_set_step, dim3(1), dim3(256), 0, s, st, step);
 }
 
 cudaError_t launch_logsoftmax_gather(const GrState& st, const float* logits, int64_t ld,
                                      float* logprobs_out, float* lse_out, const float* lse_in,
                                      cudaStream_t s) {
-    dim3 grid(st.rows * kLogitCluster);
-    k_logsoftmax_gather<<<grid, kLsThreads, 0, s>>>(st, logits, ld, logprobs_out, lse_out, lse_in);
-    return cudaGetLastError();
+    return launch(k_logsoftmax_gather, dim3(st.rows * kLogitCluster), dim3(kLsThreads), 0, s, st, logits, ld,
+                  logprobs_out, lse_out, lse_in);
 }
 
 cudaError_t launch_topk_select(const GrState& st, cudaStream_t s) {
@@ -312,18 +320,15 @@ cudaError_t launch_topk_select(const GrState& st, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    k_topk_merge<<<st.n_req * topk::kMergeCTAs, topk::kMergeThreads, kMergeSmemBytes, s>>>(st);
-    return cudaGetLastError();
+    return launch(k_topk_merge, dim3(st.n_req * topk::kMergeCTAs), dim3(topk::kMergeThreads), kMergeSmemBytes, s, st);
 }
 
 cudaError_t launch_advance(const GrState& st, cudaStream_t s) {
-    k_advance<<<st.n_req, kMaxBeam, 0, s>>>(st);
-    return cudaGetLastError();
+    return launch(k_advance, dim3(st.n_req), dim3(kMaxBeam), 0, s, st);
 }
 
 cudaError_t launch_results(const GrState& st, cudaStream_t s) {
-    k_results<<<st.n_req, kMaxBeam, 0, s>>>(st);
-    return cudaGetLastError();
+    return launch(k_results, dim3(st.n_req), dim3(kMaxBeam), 0, s, st);
 }
 
 }  // namespace grb
