@@ -353,66 +353,138 @@ k_ctx_attn(const __grid_constant__ CUtensorMap qmap, GrState st, int layer, cons
                 uint32_t sv[128];
                 tmem_ld128(tmem + lane_base + P::s_col(bs), sv);
                 const int valid = ctx_len - (J.t0 + jj) * kTileKeys;
-                if (valid < kTileKeys) {
+                auto mask = [&]() {  // keys past the context
+                    if (valid < kTileKeys) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (c >= valid) sv[c] = __float_as_uint(-CUDART_INF_F);
-                }
-                // row maximum: four independent 3-input max chains
-                float a0 = -CUDART_INF_F, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
-#pragma unroll
-                for (int c = 0; c < 128; c += 8) {
-                    a0 = fmax3(a0, __uint_as_float(sv[c + 0]), __uint_as_float(sv[c + 1]));
-                    a1 = fmax3(a1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
-                    a2 = fmax3(a2, __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
-                    a3 = fmax3(a3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
-                }
-                const float mx = fmax3(fmaxf(a0, a1), a2, a3);
-                if (jj == 0) {
-                    m_used = mx;
-                } else {
-                    const bool need = (mx - m_used) * scale_log2 > 8.f;
-                    if (__any_sync(0xffffffffu, need)) {
-                        // O holds the previous key tiles once the last PV has completed (with one
-                        // S buffer per query tile this S waited for it; with kOne it did not)
-                        if (kOne && !(ok = wait_warp(bar(B_PVD + ((tiles - 1) & 1)), ((tiles - 1) >> 1) & 1, wt)))
-                            break;
-                        tc_fence_after();
-                        const float m_new = need ? mx : m_used;
-                        const float alpha = exp2f((m_used - m_new) * scale_log2);
-#pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t ov[32];
-                            const uint32_t ta = tmem + lane_base + P::o_col(i) + 32 * c;
-                            tmem_ld32(ta, ov);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                            tmem_st32(ta, ov);
-                        }
-                        tmem_st_wait();
-                        l *= alpha;
-                        m_used = m_new;
+                        for (int c = 0; c < 128; ++c)
+                            if (c >= valid) sv[c] = __float_as_uint(-CUDART_INF_F);
                     }
+                };
+                mask();
+                if constexpr (kOne) {
+                    // The exponentials are taken relative to a reference max known before the tile: the
+                    // running max m_used (a job's first tile: the max of its first 8 columns).  The row
+                    // max comes out of the same pass.  Only when it exceeds the reference by more than
+                    // 2^8 (in exp2 units) is the tile redone relative to it (S reloaded from TMEM, O and
+                    // l rescaled): the max is off the tile's critical chain, and every p is <= 2^8.
+                    float m_ref = m_used;
+                    if (jj == 0) {
+                        m_ref = fmax3(fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2])),
+                                      fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5])),
+                                      fmaxf(__uint_as_float(sv[6]), __uint_as_float(sv[7])));
+                    }
+                    uint64_t acc[4];
+                    for (;;) {
+                        // p = 2^(s*scale_log2 - m*scale_log2), two columns per packed FMA; the row max
+                        // in four independent 3-input max chains
+                        const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+                        const uint64_t mb2 = f2_pack(-m_ref * scale_log2, -m_ref * scale_log2);
+                        float mc[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+    #pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[c] = 0ull;
+    #pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            const float s0 = __uint_as_float(sv[2 * c]), s1 = __uint_as_float(sv[2 * c + 1]);
+                            mc[c & 3] = fmax3(mc[c & 3], s0, s1);
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(s0, s1), sc2, mb2), x0, x1);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
+                            sv[c] = pack_bf16x2(p0, p1);
+                        }
+                        const float mx = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
+                        const bool need = (mx - m_ref) * scale_log2 > 8.f;
+                        if (!__any_sync(0xffffffffu, need)) break;
+                        // rare: some row's max grew past the reference
+                        const float m_new = need ? mx : m_ref;
+                        if (jj > 0) {
+                            // O holds the previous key tiles once the last PV has completed (with one
+                            // S buffer per query tile this S waited for it; with kOne it did not)
+                            if (kOne && !(ok = wait_warp(bar(B_PVD + ((tiles - 1) & 1)), ((tiles - 1) >> 1) & 1, wt)))
+                                break;
+                            tc_fence_after();
+                            const float alpha = exp2f((m_ref - m_new) * scale_log2);
+    #pragma unroll 1
+                            for (int c = 0; c < D / 32; ++c) {
+                                uint32_t ov[32];
+                                const uint32_t ta = tmem + lane_base + P::o_col(i) + 32 * c;
+                                tmem_ld32(ta, ov);
+    #pragma unroll
+                                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                                tmem_st32(ta, ov);
+                            }
+                            tmem_st_wait();
+                            l *= alpha;
+                        }
+                        m_ref = m_new;
+                        tmem_ld128(tmem + lane_base + P::s_col(bs), sv);  // S is still there: P is stored below
+                        mask();
+                    }
+                    if (!ok) break;
+                    m_used = m_ref;
+                    float t0, t1, t2, t3, t4, t5, t6, t7;
+                    f2_unpack(acc[0], t0, t1);
+                    f2_unpack(acc[1], t2, t3);
+                    f2_unpack(acc[2], t4, t5);
+                    f2_unpack(acc[3], t6, t7);
+                    l += ((t0 + t1) + (t2 + t3)) + ((t4 + t5) + (t6 + t7));
+                } else {
+                    // row maximum: four independent 3-input max chains
+                    float a0 = -CUDART_INF_F, a1 = -CUDART_INF_F, a2 = -CUDART_INF_F, a3 = -CUDART_INF_F;
+    #pragma unroll
+                    for (int c = 0; c < 128; c += 8) {
+                        a0 = fmax3(a0, __uint_as_float(sv[c + 0]), __uint_as_float(sv[c + 1]));
+                        a1 = fmax3(a1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+                        a2 = fmax3(a2, __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+                        a3 = fmax3(a3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+                    }
+                    const float mx = fmax3(fmaxf(a0, a1), a2, a3);
+                    if (jj == 0) {
+                        m_used = mx;
+                    } else {
+                        const bool need = (mx - m_used) * scale_log2 > 8.f;
+                        if (__any_sync(0xffffffffu, need)) {
+                            // O holds the previous key tiles once the last PV has completed (with one
+                            // S buffer per query tile this S waited for it; with kOne it did not)
+                            if (kOne && !(ok = wait_warp(bar(B_PVD + ((tiles - 1) & 1)), ((tiles - 1) >> 1) & 1, wt)))
+                                break;
+                            tc_fence_after();
+                            const float m_new = need ? mx : m_used;
+                            const float alpha = exp2f((m_used - m_new) * scale_log2);
+    #pragma unroll 1
+                            for (int c = 0; c < D / 32; ++c) {
+                                uint32_t ov[32];
+                                const uint32_t ta = tmem + lane_base + P::o_col(i) + 32 * c;
+                                tmem_ld32(ta, ov);
+    #pragma unroll
+                                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                                tmem_st32(ta, ov);
+                            }
+                            tmem_st_wait();
+                            l *= alpha;
+                            m_used = m_new;
+                        }
+                    }
+                    // p = 2^(s*scale_log2 - m*scale_log2), two columns per packed FMA
+                    const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+                    const uint64_t mb2 = f2_pack(-m_used * scale_log2, -m_used * scale_log2);
+                    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+    #pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), sc2, mb2),
+                                  x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
+                        sv[c] = pack_bf16x2(p0, p1);
+                    }
+                    float s0, s1, s2, s3, s4, s5, s6, s7;
+                    f2_unpack(acc[0], s0, s1);
+                    f2_unpack(acc[1], s2, s3);
+                    f2_unpack(acc[2], s4, s5);
+                    f2_unpack(acc[3], s6, s7);
+                    l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
                 }
-                // p = 2^(s*scale_log2 - m*scale_log2), two columns per packed FMA
-                const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
-                const uint64_t mb2 = f2_pack(-m_used * scale_log2, -m_used * scale_log2);
-                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), sc2, mb2),
-                              x0, x1);
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    acc[c & 3] = f2_add(acc[c & 3], f2_pack(p0, p1));
-                    sv[c] = pack_bf16x2(p0, p1);
-                }
-                float s0, s1, s2, s3, s4, s5, s6, s7;
-                f2_unpack(acc[0], s0, s1);
-                f2_unpack(acc[1], s2, s3);
-                f2_unpack(acc[2], s4, s5);
-                f2_unpack(acc[3], s6, s7);
-                l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
                 tmem_st32(tmem + lane_base + P::p_col(bs), sv);
                 tmem_st32(tmem + lane_base + P::p_col(bs) + 32, sv + 32);
                 tmem_st_wait();

@@ -86,3 +86,15 @@ def test_one_tile_units_many_jobs_per_cta():
                 widths=[30] * 24, n_items=[4000] * 24, seed=93)
     _, res = _run(spec, steps=2)
     assert max(r["worst"] for r in res) <= 1.0, res
+
+
+@pytest.mark.parametrize("q_std", [4.0, 16.0])
+def test_two_tile_units_with_growing_row_max(q_std):
+    # two query tiles per unit (beam 256 x 2 query heads); spread query scales make a row's max
+    # grow past the running reference on later key tiles, so tiles are redone relative to the
+    # new max (O and the sums rescaled) -- including on a job's first tile
+    spec = Spec(n_layers=1, n_q_heads=4, n_kv_heads=2, head_dim=128, vocab=4096, n_levels=3,
+                codes_per_level=256, code_base=4096 - 768, ctx_lens=[3000, 700], widths=[256, 256],
+                n_items=[60000] * 2, q_std=q_std, seed=97)
+    _, res = _run(spec, steps=2)
+    assert max(r["worst"] for r in res) <= 1.0, res
