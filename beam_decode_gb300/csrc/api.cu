@@ -475,7 +475,7 @@ WsLayout ws_layout(const gr_config* c, int n, int rows, const Caps& k) {
     w.sel_key = take(4ull * rows);
     w.n_sel = take(4ull * n);
     w.status = take(16);
-    w.key_range = take(8ull * n);
+    w.key_range = take(16ull * n);
     w.o_part = take(4ull * k.jobs * kUnitRows * c->head_dim);
     w.lse_part = take(4ull * k.jobs * kUnitRows);
     w.piece_flag = take(4ull * k.jobs * kUnitRows);

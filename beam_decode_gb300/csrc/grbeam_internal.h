@@ -98,7 +98,7 @@ struct GrState {
     float* sel_key;     // [rows]
     int32_t* n_sel;     // [n_req]
     int32_t* status;    // [4]
-    uint32_t* key_range;// [n_req][2] (~lower, upper) bound of the step's candidate keys (top-K)
+    uint32_t* key_range;// [n_req][4] (~lower, upper, ~smallest row maximum, unused) of the step's candidate keys (top-K)
 
     // attention
     CUtensorMap* tmaps; // [n_req][kTmapsPerReq] (K, V, K half tiles) of the ContextKV pool

@@ -36,8 +36,9 @@ namespace cg = cooperative_groups;
 constexpr int kNaMaxCandidates = GR_NOALLOC_MAX_CANDIDATES;
 constexpr size_t kNaKeysBytes = 4ull * kNaMaxCandidates;  // ordered candidate keys [n_rows][n_codes]
 
-// Scratch of the no-alloc path: the candidate keys, then the (~lower, upper) bound of them
-// that the first kernel raises and the second reads and clears (zero at load).
+// Scratch of the no-alloc path: the candidate keys, then three bound words of them (~lower,
+// upper, ~smallest row maximum) that the first kernel raises and the second reads and clears
+// (zero at load).
 // Host code must not use this name as an address (it is a host-side stand-in);
 // the device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNaKeysBytes + 256];

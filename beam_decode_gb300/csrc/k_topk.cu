@@ -94,7 +94,7 @@ k_logsoftmax_gather(GrState st, const float* __restrict__ logits, int64_t ld,
     const uint32_t* mk = R.mask + node * R.mask_words;
     const float* xc = x + st.code_base + (int64_t)t * C;
     const bool nan = topk::gather_row(xc, mk, S, lse, C, R.width, part, row_keys, st.cand + (int64_t)row * C,
-                                      st.key_range + 2 * r, [&](int c, bool valid, float lp) {
+                                      st.key_range + 4 * r, [&](int c, bool valid, float lp) {
                                           if (logprobs_out != nullptr)
                                               logprobs_out[(int64_t)row * C + c] = valid ? lp : -CUDART_INF_F;
                                       });
@@ -119,7 +119,7 @@ k_topk_merge(GrState st) {
     const int n_live = st.n_beams[r * (st.n_levels + 1) + t];
     const topk::MergeOut out{st.sel_parent + R.row_off, st.sel_code + R.row_off, st.sel_key + R.row_off,
                              st.n_sel + r};
-    topk::merge_select(st.cand + (int64_t)R.row_off * C, n_live * C, C, R.width, st.key_range + 2 * r, out, stage,
+    topk::merge_select(st.cand + (int64_t)R.row_off * C, n_live * C, C, R.width, st.key_range + 4 * r, out, stage,
                        sm);
 }
 
@@ -194,7 +194,7 @@ __global__ void k_init_state(GrState st) {
         st.n_beams[i] = (i % L1 == 0) ? 1 : 0;
     for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < st.n_req; r += gridDim.x * blockDim.x) st.req_step[r] = 0;
     if (blockIdx.x == 0 && threadIdx.x < 4) st.status[threadIdx.x] = 0;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 2 * st.n_req; i += gridDim.x * blockDim.x)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 4 * st.n_req; i += gridDim.x * blockDim.x)
         st.key_range[i] = 0u;
 }
 

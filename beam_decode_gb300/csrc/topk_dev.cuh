@@ -21,16 +21,19 @@
 //   stage 2 (cross-beam merge, one cluster of kMergeCTAs CTAs per request):
 //     each CTA takes a contiguous flat range of the request's keys into shared
 //     memory.  The threshold -- the W-th largest key -- is found by
-//     range-adaptive bucketing: kNB equal-width buckets over [smallest,
-//     largest] key; each CTA counts its keys into a shared histogram, and
-//     after a cluster barrier every CTA sums the CTAs' histograms through
-//     distributed shared memory and finds the same bucket holding the W-th
-//     key.  While that bucket holds more than kThrCap keys (and more than one
-//     key value) it is bucketed again (four levels of 8 bits cover 32).  Keys
-//     above the bucket are taken; the bucket's keys are collected and its top
-//     kk (key desc, flat asc) taken too; each taken entry's output position
-//     is its rank among them.  A bucket of more than kThrCap equal keys takes
-//     its first kk in flat order instead.  Every exchange goes through the
+//     range-adaptive bucketing: kNB equal-width buckets over [a0, largest
+//     key], where a0 is the smallest key, or, when the request has at least W
+//     rows, the smallest of the rows' largest keys if that is higher (those W
+//     maxima lie at or above it, so the W-th largest key does too); each warp
+//     counts its keys into its own histogram, and after a cluster barrier
+//     every CTA sums the CTAs' histograms through distributed shared memory
+//     and finds the same bucket holding the W-th key.  While that bucket
+//     holds more than kThrCap keys (and more than one key value) it is
+//     bucketed again (levels of kNBBits bits cover 32).  Keys above the
+//     bucket are taken; the bucket's keys are collected and its top kk (key
+//     desc, flat asc) taken too; each taken entry's output position is its
+//     rank among them.  A bucket of more than kThrCap equal keys takes its
+//     first kk in flat order instead.  Every exchange goes through the
 //     cluster's shared memory: the merge needs no global scratch.
 #pragma once
 
@@ -165,7 +168,8 @@ __device__ __forceinline__ uint32_t row_keep(const uint32_t* row_keys, int C, in
 // keep < C, and this CTA's quarter of the row written to out[0..C).  on_code(c, valid, lp)
 // is called for the CTA's codes (lp = x - LSE).  The request's bound of candidate keys,
 // range[0..1] = (~lower, upper), is raised to cover them (fire-and-forget atomics, one pair
-// per warp that formed keys).  Returns whether a valid key was NaN.  Every thread of the CTA
+// per warp of the row's first CTA), and range[2] to ~(this row's largest key): over the
+// request's rows it holds ~(the smallest row maximum).  Returns whether a valid key was NaN.  Every thread of the CTA
 // calls it; row_keys is kMaxCodes uint32 of shared memory.
 template <typename OnCode>
 __device__ __forceinline__ bool gather_row(const float* __restrict__ xc, const uint32_t* __restrict__ mk, float S,
@@ -173,12 +177,12 @@ __device__ __forceinline__ bool gather_row(const float* __restrict__ xc, const u
                                            uint32_t* __restrict__ out, uint32_t* range, OnCode&& on_code) {
     const int c0 = (int)((int64_t)C * part / kLogitCluster);
     const int c1 = (int)((int64_t)C * (part + 1) / kLogitCluster);
-    // stage 1 needs every key of the row in each CTA; without it each CTA forms only its quarter
     const bool prune = keep < C;
-    const int f0 = prune ? 0 : c0, f1 = prune ? C : c1;
+    // Every CTA forms all C keys of the row: stage 1 ranks each against the whole row, and the
+    // row's largest key feeds the bound below.  Only this CTA's quarter is written.
     bool nan = false;
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    for (int c = f0 + (int)threadIdx.x; c < f1; c += kLsThreads) {
+    for (int c = (int)threadIdx.x; c < C; c += kLsThreads) {
         const bool valid = (mk[c >> 5] >> (c & 31)) & 1u;
         const float x = xc[c];
         const uint32_t u = candidate_key(S, x, lse, valid, &nan);
@@ -186,9 +190,8 @@ __device__ __forceinline__ bool gather_row(const float* __restrict__ xc, const u
             lo = min(lo, u);
             hi = max(hi, u);
         }
-        if (prune) {
-            row_keys[c] = u;
-        } else {
+        row_keys[c] = u;
+        if (!prune && c >= c0 && c < c1) {
             out[c] = u;
             on_code(c, valid, __fsub_rn(x, lse));
         }
@@ -198,12 +201,24 @@ __device__ __forceinline__ bool gather_row(const float* __restrict__ xc, const u
         lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
         hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
     }
-    if ((threadIdx.x & 31) == 0 && hi != 0u && (!prune || part == 0)) {
-        atomicMax(range, ~lo);
-        atomicMax(range + 1, hi);
+    __shared__ uint32_t warp_hi[kLsThreads / 32];
+    if ((threadIdx.x & 31) == 0) {
+        warp_hi[threadIdx.x >> 5] = hi;
+        if (hi != 0u && part == 0) {
+            atomicMax(range, ~lo);
+            atomicMax(range + 1, hi);
+        }
+    }
+    __syncthreads();
+    if (part == 0 && threadIdx.x == 0) {
+        // range[2] = ~(the smallest of the rows' largest keys); a row without a candidate
+        // counts as 0, which turns the bound off
+        uint32_t m = 0u;
+#pragma unroll
+        for (int k = 0; k < kLsThreads / 32; ++k) m = max(m, warp_hi[k]);
+        atomicMax(range + 2, ~m);
     }
     if (prune) {
-        __syncthreads();
         for (int c = c0 + (int)threadIdx.x; c < c1; c += kLsThreads) {
             out[c] = row_keep(row_keys, C, c, keep);  // the beam's own top `keep`
             on_code(c, (mk[c >> 5] >> (c & 31)) & 1u, __fsub_rn(xc[c], lse));
@@ -216,21 +231,24 @@ __device__ __forceinline__ bool gather_row(const float* __restrict__ xc, const u
 // stage 2: cross-beam merge
 // ---------------------------------------------------------------------------
 constexpr int kMergeCTAs = 8;         // one portable cluster per request
-constexpr int kMergeThreads = 256;
+constexpr int kNBBits = 8;
+constexpr int kNB = 1 << kNBBits;     // buckets per level (one per thread)
+constexpr int kMergeThreads = kNB;
 constexpr int kMergeStage = 16384;    // keys of a CTA's range kept in shared memory (else re-read)
-constexpr int kNB = 256;              // buckets per level (one per thread)
-constexpr int kLevels = 4;            // 256^4 = 2^32: the fourth level's buckets are single values
+// levels of kNBBits bits cover the 32-bit key: the last level's buckets are single values
+constexpr int kLevels = (32 + kNBBits - 1) / kNBBits;
 constexpr int kThrCap = 1024;         // threshold-bucket keys ranked directly
 
 // Shared memory of a merge CTA (dynamic, followed by kMergeStage staged keys).  The fields
 // other CTAs of the cluster read are marked "published".
 struct MergeSmem {
     int hist[2][kNB];                   // published: this CTA's bucket counts, by level parity
-    int hloc[kNB];                      // the counts while they are being added up
+    int hsub[kMergeThreads / 32][kNB];  // each warp's counts while they are being added up
     unsigned long long sure[kMaxBeam];  // published: this CTA's keys above the bucket, unordered
     unsigned long long thr[kThrCap];    // published: this CTA's keys in the bucket, unordered
     unsigned long long all[kMaxBeam + kThrCap];  // the cluster's lists, gathered for ranking
     int warp_tot[32];
+    int wcnt[2][kMergeThreads / 32];    // each warp's keys above the bucket / in it
     int n_sure, n_thr;                  // published: lengths of sure / thr (tie path: keys equal)
     int off_s[kMergeCTAs], off_t[kMergeCTAs], len_s[kMergeCTAs], len_t[kMergeCTAs];
     int digit, kk, dcount;
@@ -281,11 +299,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)
 __device__ __forceinline__ void smem_add(int* p, int v) {
     asm volatile("red.shared.add.s32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
-__device__ __forceinline__ int smem_fetch_add(int* p, int v) {
-    int old;
-    asm volatile("atom.shared.add.s32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v) : "memory");
-    return old;
-}
 // address of the same shared-memory object in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t peer_addr(const void* p, int rank) {
     uint32_t r;
@@ -306,9 +319,10 @@ __device__ __forceinline__ unsigned long long peer_ld64(uint32_t a) {
 // The top-min(k_want, #candidates) of N ordered keys (flat order, 0 = no candidate) of one
 // request, in (key desc, flat asc) order.  Called by every CTA of a kMergeCTAs cluster with
 // the same arguments; `stage` is kMergeStage uint32 of shared memory.  range[0..1] =
-// (~lower, upper) bound of the candidate keys, raised by stage 1 (raise_range); any bound
-// that contains every candidate gives the same result.  The merge sets it back to (0, 0)
-// for the next call once every CTA has read it.
+// (~lower, upper) bound of the candidate keys and range[2] = ~(the smallest of the N / C rows'
+// largest keys), all raised by stage 1 (gather_row); any bounds that contain every candidate
+// and lie at or below that smallest maximum give the same result.  The merge sets the three
+// words back to 0 for the next call once every CTA has read them.
 __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, int N, int C, int k_want,
                                              uint32_t* __restrict__ range, const MergeOut out, uint32_t* stage,
                                              MergeSmem& sm) {
@@ -353,10 +367,10 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
 
     // ---- stage the range with every load in flight (16-byte loads where aligned)
     const uint32_t r_lo = ~__ldcg(range), r_hi = __ldcg(range + 1);
-    if (tid == 0) {
-        sm.n_sure = 0;
-        sm.n_thr = 0;
-    }
+    // With at least k_want rows, the rows' largest keys are k_want distinct candidates at or
+    // above the smallest of them, so the k_want-th largest key is too: the keys below that
+    // bound cannot be selected and no pass counts or collects them.
+    const uint32_t a0 = max(r_lo, N / C >= k_want ? ~__ldcg(range + 2) : 0u);
     if (staged) {
         const int head = min(n, (int)((4 - ((reinterpret_cast<uintptr_t>(g) >> 2) & 3)) & 3));
         if (tid < head) stage[tid] = __ldcg(g + tid);
@@ -386,46 +400,68 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
     // The first level's counts also give the number of candidates: when it is at most k_want
     // every candidate is taken (take_all: a = b = 2^32 - 1, no bucket).
     bool take_all = r_lo > r_hi;  // no candidate in this call
-    int n_valid = 0;
-    uint32_t a = r_lo, b = r_hi;
+    int n_valid = 0;              // candidates at or above a0
+    uint32_t a = a0, b = r_hi;
     int kk = k_want, c_d = 0;
+    // Each warp counts into its own histogram, so that it also knows how many of its keys lie
+    // above the final bucket (the sum, over the levels, of its counts above the chosen bucket)
+    // and in it: the collect pass then needs no counting pass of its own.
+    constexpr int kWarps = kMergeThreads / 32;
+    const int lane = tid & 31, wid = tid >> 5;
+    const int jb = kNB - 1 - tid;  // this thread's bucket in the cluster-wide counts
+    int sure_w = 0, thr_w = 0;     // this warp's keys above the bucket and in it (warp-uniform)
+    auto warp_count_from = [&](int j0) {
+        int c = 0;
+        for (int j = j0 + lane; j < kNB; j += 32) c += sm.hsub[wid][j];
+        return (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
+    };
     if (!take_all) {
         for (int level = 0; level < kLevels; ++level) {
             // buckets of 2^sh keys: the smallest power of two with (b - a) >> sh < kNB
-            const uint32_t span = (b - a) >> 8;  // kNB = 2^8
+            const uint32_t span = (b - a) >> kNBBits;
             const int sh = span == 0u ? 0 : 32 - __clz(span);
             const uint32_t width = 1u << sh;
             int* h = sm.hist[level & 1];  // its last readers passed the previous level's barrier
-            sm.hloc[tid] = 0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) sm.hsub[w][tid] = 0;
             __syncthreads();
+            int* hw = sm.hsub[wid];
             for_keys([&](int, uint32_t u) {
-                if (u >= a && u <= b) smem_add(&sm.hloc[(u - a) >> sh], 1);
+                if (u >= a && u <= b) smem_add(&hw[(u - a) >> sh], 1);
             });
             __syncthreads();
-            h[tid] = sm.hloc[tid];  // published with a plain store
+            {
+                int cnt = 0;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) cnt += sm.hsub[w][tid];
+                h[tid] = cnt;  // published with a plain store
+            }
             cl.sync();
             // the cluster's count of bucket tid, then the bucket of the kk-th key (thread order
             // is descending bucket order)
             int tsum = 0;
 #pragma unroll
-            for (int r = 0; r < kMergeCTAs; ++r) tsum += peer_ld(peer_addr(&h[kNB - 1 - tid], r));
+            for (int r = 0; r < kMergeCTAs; ++r) tsum += peer_ld(peer_addr(&h[jb], r));
             int total;
             const int incl = block_incl_scan(tsum, sm.warp_tot, total);
             if (level == 0) {
                 n_valid = total;
                 if (total <= k_want) {
                     take_all = true;
+                    sure_w = warp_count_from(0);
                     break;
                 }
             }
             if (incl - tsum < kk && kk <= incl) {
-                sm.digit = kNB - 1 - tid;
+                sm.digit = jb;
                 sm.kk = kk - (incl - tsum);
                 sm.dcount = tsum;
             }
             __syncthreads();
             const int d = sm.digit;
             c_d = sm.dcount;
+            sure_w += warp_count_from(d + 1);
+            thr_w = sm.hsub[wid][d];
             const uint32_t na = a + (uint32_t)d * width;
             b = (b - na < width - 1u) ? b : na + (width - 1u);
             a = na;
@@ -444,15 +480,69 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
     const bool ranked = c_d <= kThrCap;      // else: one key value, its first kk in flat order
 
     // ---- collect: this CTA's keys above the bucket into `sure`, the bucket's keys into `thr`
-    // (tie path: only counted), in any order
-    for_keys([&](int i, uint32_t u) {
-        if (u != 0u && (take_all || u > b)) {
-            sm.sure[smem_fetch_add(&sm.n_sure, 1)] = sel_entry(u, lo + i);
-        } else if (!take_all && u >= a && u <= b) {
-            const int p = smem_fetch_add(&sm.n_thr, 1);
-            if (ranked) sm.thr[p] = sel_entry(u, lo + i);
+    // (tie path: only counted), in flat order within each warp's share, from the warp's offset
+    // on (the warps' counts come from their histograms; a shared counter that every warp
+    // appended to would serialise the warps).
+    auto classify = [&](uint32_t u, bool& is_s, bool& is_t) {
+        is_s = u >= a0 && (take_all || u > b);  // a0 >= 1: no 0 (no candidate) qualifies
+        is_t = !take_all && !is_s && u >= a;    // then u <= b
+    };
+    // (the staged and the global loop are kept apart: a select between a shared and a global
+    // load per key would put a global round trip on every iteration)
+    auto for_keys_warp = [&](auto&& f) {
+        if (staged) {
+            for (int base = 0; base < n; base += 4 * kMergeThreads) {
+                uint32_t v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = base + k * kMergeThreads + tid;
+                    v[k] = i < n ? stage[i] : 0u;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) f(base + k * kMergeThreads + tid, v[k]);
+            }
+        } else {
+            for (int base = 0; base < n; base += kMergeBatch * kMergeThreads) {
+                uint32_t v[kMergeBatch];
+#pragma unroll
+                for (int k = 0; k < kMergeBatch; ++k) {
+                    const int i = base + k * kMergeThreads + tid;
+                    v[k] = i < n ? __ldcg(g + i) : 0u;
+                }
+#pragma unroll
+                for (int k = 0; k < kMergeBatch; ++k) f(base + k * kMergeThreads + tid, v[k]);
+            }
         }
-    });
+    };
+    {
+        if (lane == 0) {
+            sm.wcnt[0][wid] = sure_w;
+            sm.wcnt[1][wid] = thr_w;
+        }
+        __syncthreads();
+        int os = 0, ot = 0, ts = 0, tt = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            os += w < wid ? sm.wcnt[0][w] : 0;
+            ot += w < wid ? sm.wcnt[1][w] : 0;
+            ts += sm.wcnt[0][w];
+            tt += sm.wcnt[1][w];
+        }
+        if (tid == 0) {
+            sm.n_sure = ts;
+            sm.n_thr = tt;
+        }
+        const unsigned lt = (1u << lane) - 1u;
+        for_keys_warp([&](int i, uint32_t u) {
+            bool is_s, is_t;
+            classify(u, is_s, is_t);
+            const unsigned bs = __ballot_sync(0xffffffffu, is_s), bt = __ballot_sync(0xffffffffu, is_t);
+            if (is_s) sm.sure[os + __popc(bs & lt)] = sel_entry(u, lo + i);
+            if (is_t && ranked) sm.thr[ot + __popc(bt & lt)] = sel_entry(u, lo + i);
+            os += __popc(bs);
+            ot += __popc(bt);
+        });
+    }
     cl.sync();
     // gather every CTA's lists (offsets in cluster rank order)
     if (tid < kMergeCTAs) {
@@ -491,8 +581,9 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
     }
     cl.sync();  // no CTA leaves while another still reads its lists
     if (cr == 0 && tid == 0) {
-        range[0] = 0u;  // every CTA has read the bound: clear it for the next call
+        range[0] = 0u;  // every CTA has read the bounds: clear them for the next call
         range[1] = 0u;
+        range[2] = 0u;
     }
 
     auto emit = [&](int pos, unsigned long long e) {
@@ -529,8 +620,10 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
             const bool act = e < r1;
             const unsigned long long me = act ? list[e] : 0ull;
             int above = 0;
-            if (act)
+            if (act) {
+#pragma unroll 4
                 for (int j = part; j < len; j += kSplit) above += list[j] > me;
+            }
 #pragma unroll
             for (int off = kSplit / 2; off > 0; off >>= 1) above += __shfl_xor_sync(0xffffffffu, above, off);
             if (act && part == 0 && above < limit) emit(pos0 + above, me);

@@ -441,13 +441,14 @@ gr_status gr_beam_attn_kernel(const gr_beam* beam, int* pair);
  *   out_n        device int32 [1]: number written
  * Limits: n_rows * n_codes <= GR_NOALLOC_MAX_CANDIDATES, n_codes <= 1024,
  * k <= 1024; larger sizes return GR_ERR_CAPACITY and launch nothing.
- * Scratch: the candidate keys and the candidates' key range live in one
+ * Scratch: the candidate keys and three words of bounds on them (their
+ * key range and the smallest of the rows' largest keys) live in one
  * fixed device array of the library (GR_NOALLOC_MAX_CANDIDATES x 4 bytes =
  * 1 MiB, plus 256 bytes) that every GPU which loads the library holds until
  * the process exits.  The call allocates nothing: no cudaMalloc, no
- * cudaFree, no allocating library routine.  The key range must start at
- * zero: it does when the library is loaded, and every call's last kernel
- * clears it again.  Every call on a device shares that one array and
+ * cudaFree, no allocating library routine.  The bound words must start at
+ * zero: they do when the library is loaded, and every call's last kernel
+ * clears them again.  Every call on a device shares that one array and
  * overwrites it, so calls that overlap on the GPU (concurrent streams, or
  * several host threads) race and must be serialised by the caller; calls
  * queued on one stream are fine.  Each call looks the array's device address

@@ -96,3 +96,36 @@ def test_all_keys_equal_uses_global_path():
     for t in range(2):
         r = ls.topk_step(lse_mode=True)
         assert not r["mismatch"], (t, r)
+
+
+def test_row_without_candidates_turns_the_threshold_bound_off():
+    """With at least W live rows the merge skips every key below the smallest row maximum (the
+    rows' maxima are W candidates at or above it); a row without candidates has no maximum and
+    must turn that bound off.  At level 1 every row gets one dominant valid code, so the rows'
+    maxima are the only keys near the top.  One row's codes are NaN on the GPU (not candidates)
+    and -inf for the oracle (candidates it never ranks among the first W here).  A bound taken
+    over the other rows alone would leave only their W - 1 maxima and return W - 1 beams."""
+    import torch
+    from beam_decode_gb300 import binding as B
+    W = 32
+    spec = Spec(vocab=4096, n_levels=2, codes_per_level=64, code_base=4096 - 128, widths=[W],
+                n_items=[3000], seed=27)
+    ls = LockStep(spec)
+    r = ls.topk_step(lse_mode=True)
+    assert not r["mismatch"] and r["n_sel"] == [W], r
+    ob = ls.obeams[0]
+    x = ls.logits(1)
+    lo = spec.code_base + spec.codes_per_level
+    for b, pre in enumerate(ob.prefixes()):
+        x[b, lo + ob.trie.valid_codes(pre)[0]] = 40.0
+    dead = 5
+    x_or, x_gpu = x.copy(), x.copy()
+    x_or[dead, lo:lo + spec.codes_per_level] = -np.inf
+    x_gpu[dead, lo:lo + spec.codes_per_level] = np.nan
+    oinfo, lse32 = ls.oracle_topk(x_or)
+    lse_in = torch.from_numpy(np.nan_to_num(lse32, nan=0.0)).cuda()
+    ls.beam.constrained_topk(torch.from_numpy(x_gpu).cuda(), ld=x.shape[1], lse_in=lse_in)
+    ls.beam.advance()
+    assert ls.beam.status(clear=True) == B.GR_ERR_DEVICE  # the NaN keys are reported
+    res = ls.compare_topk(oinfo, lse_mode=True)
+    assert not res["mismatch"] and res["n_sel"] == [W], res
