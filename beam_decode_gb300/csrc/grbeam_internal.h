@@ -20,7 +20,7 @@ constexpr int kMaxPriv = 16;          // private keys of one query row (BeamKV p
 constexpr int kTileRows = 128;        // query rows per tensor-core tile (TMEM lanes)
 constexpr int kTileKeys = 128;        // context keys per tile
 constexpr int kUnitRows = 256;        // query rows per attention unit (two tiles)
-constexpr int kLogitCluster = 4;      // CTAs sharing one logit row
+constexpr int kLogitCluster = 2;      // CTAs sharing one logit row
 constexpr int kTmapsPerReq = 3;       // ContextKV tensor maps of a request: K, V, K in half tiles of 64 keys
 
 // status word bits (device)

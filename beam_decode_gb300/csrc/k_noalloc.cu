@@ -15,7 +15,7 @@
 // key(b, c) = S_b + (x[b][code_lo + c] - LSE_b) over the codes c whose bit is
 // set in the row's mask, ordered by key descending then flat index b*C + c
 // ascending, the first min(k, #candidates) kept.  Both entry points run the
-// same device code (topk_dev.cuh: the four-CTA log-sum-exp of each row, the
+// same device code (topk_dev.cuh: the clustered log-sum-exp of each row, the
 // key encoding, the per-beam stage 1 and the cross-beam merge), so they
 // return identical selections and keys for identical inputs.
 #include <cuda_runtime.h>
@@ -43,7 +43,7 @@ constexpr size_t kNaKeysBytes = 4ull * kNaMaxCandidates;  // ordered candidate k
 // the device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNaKeysBytes + 256];
 
-// one 4-CTA cluster per row: row log-sum-exp, then the masked keys of the codes (stage 1
+// one kLogitCluster-CTA cluster per row: row log-sum-exp, then the masked keys of the codes (stage 1
 // keeps each row's own top `keep`)
 __global__ void __cluster_dims__(kLogitCluster, 1, 1) __launch_bounds__(topk::kLsThreads, 8)
 k_na_logsoftmax_gather(const float* __restrict__ logits, int64_t ld, int vocab, int code_lo, int n_codes,

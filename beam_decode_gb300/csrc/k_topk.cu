@@ -8,7 +8,7 @@
 // "Background: what inference a recommendation request needs").
 //
 // Kernels
-//   k_logsoftmax_gather  one pass over each live logit row (a cluster of 4 CTAs
+//   k_logsoftmax_gather  one pass over each live logit row (a cluster of 2 CTAs
 //                        per row): log-sum-exp of the full vocabulary, then the
 //                        level's C code logits -> masked float32 keys
 //                        key = S_b + (x - LSE_b), stored as order-preserving
@@ -82,7 +82,7 @@ k_logsoftmax_gather(GrState st, const float* __restrict__ logits, int64_t ld,
     }
     if (part == 0 && threadIdx.x == 0 && lse_out != nullptr) lse_out[row] = lse;
 
-    // level gather of the C codes (stage 1 of the top-K included), a quarter of the row per CTA
+    // level gather of the C codes (stage 1 of the top-K included), a part of the row per CTA
     const GrReqDev& R = st.req[r];
     const int C = st.C;
     const int64_t node = (t == 0) ? 0 : st.node[(int64_t)(t - 1) * st.rows + row];

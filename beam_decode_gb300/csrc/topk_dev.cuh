@@ -71,8 +71,8 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
 constexpr int kLsThreads = 256;  // threads of a log-softmax CTA
 
 // Natural-log log-sum-exp of one logit row of V floats (16-byte aligned), split over the
-// kLogitCluster CTAs of a cluster: each CTA reduces a quarter of the row with 16-byte loads
-// into a running (max, sum), the cluster combines the four partials through distributed
+// kLogitCluster CTAs of a cluster: each CTA reduces its part of the row with 16-byte loads
+// into a running (max, sum), the cluster combines the partials through distributed
 // shared memory in a fixed order, and every CTA returns the same value.
 __device__ __forceinline__ float cluster_row_lse(const float* __restrict__ x, int V, cg::cluster_group& cluster,
                                                  int part, float* red_m, float* red_s, float* part_ms) {
@@ -124,7 +124,7 @@ __device__ __forceinline__ float cluster_row_lse(const float* __restrict__ x, in
         part_ms[1] = ss;
     }
     cluster.sync();
-    // every CTA combines the four partials in the same order
+    // every CTA combines the partials in the same order
     float mm = -CUDART_INF_F, ss = 0.f;
     for (int k = 0; k < kLogitCluster; ++k) {
         const float* pk = cluster.map_shared_rank(part_ms, k);
@@ -165,7 +165,7 @@ __device__ __forceinline__ uint32_t row_keep(const uint32_t* row_keys, int C, in
 // The level gather of one live row for one CTA of its kLogitCluster cluster (`part`): the
 // candidate keys of the C codes (xc = the row's logits of the level's codes, mk = the row's
 // mask of valid codes, S = the beam's score, lse = the row's log-sum-exp), stage 1 when
-// keep < C, and this CTA's quarter of the row written to out[0..C).  on_code(c, valid, lp)
+// keep < C, and this CTA's part of the row written to out[0..C).  on_code(c, valid, lp)
 // is called for the CTA's codes (lp = x - LSE).  The request's bound of candidate keys,
 // range[0..1] = (~lower, upper), is raised to cover them (fire-and-forget atomics, one pair
 // per warp of the row's first CTA), and range[2] to ~(this row's largest key): over the
@@ -179,7 +179,7 @@ __device__ __forceinline__ bool gather_row(const float* __restrict__ xc, const u
     const int c1 = (int)((int64_t)C * (part + 1) / kLogitCluster);
     const bool prune = keep < C;
     // Every CTA forms all C keys of the row: stage 1 ranks each against the whole row, and the
-    // row's largest key feeds the bound below.  Only this CTA's quarter is written.
+    // row's largest key feeds the bound below.  Only this CTA's part is written.
     bool nan = false;
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
     for (int c = (int)threadIdx.x; c < C; c += kLsThreads) {
