@@ -318,6 +318,13 @@ def batched_cpu_step_seconds(w: wl.Workload):
     return per_step, threads, sample
 
 
+def workload_config(w):
+    """The workload keys of the JSON line's config, the same for both arms."""
+    return {"workload": w.name, "requests": w.n_requests, "ctx": w.ctx_lens[0], "beam": w.beam_widths[0],
+            "layers": w.n_layers, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+            "vocab": w.vocab, "levels": w.n_levels, "codes": w.codes_per_level, "items": w.n_items[0]}
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -334,8 +341,7 @@ def run_reference(args, w):
     line = {"metric": METRIC, "value": value, "unit": "steps/s", "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "requests": w.n_requests, "ctx": w.ctx_lens[0], "beam": w.beam_widths[0],
-                       "levels": w.n_levels, "codes": w.codes_per_level, "vocab": w.vocab},
+            "config": dict(workload_config(w), parallelism="oracle, one host core"),
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -486,12 +492,10 @@ def run_gpu(args, w):
         line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": w.name, "requests": w.n_requests, "ctx": w.ctx_lens[0],
-                           "beam": w.beam_widths[0], "layers": w.n_layers, "q_heads": w.n_q_heads,
-                           "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "vocab": w.vocab,
-                           "levels": w.n_levels, "codes": w.codes_per_level, "items": w.n_items[0],
-                           "l2": "inputs larger than L2 (ContextKV %.2f GB)" % (batch.ctx_bytes_per_layer() * w.n_layers / 1e9), "parallelism": f"replicas{world}",
-                           "cuda_graph": not args.no_graph, "attn_kernel": beam.attn_kernel()},
+                "config": dict(workload_config(w),
+                               l2="inputs larger than L2 (ContextKV %.2f GB)" % (batch.ctx_bytes_per_layer() * w.n_layers / 1e9),
+                               parallelism=f"replicas{world}", cuda_graph=not args.no_graph,
+                               attn_kernel=beam.attn_kernel()),
                 "eager": {"value": job_value(ms_eager / args.steps, world), "unit": "steps/s",
                           "ms_per_step": ms_eager / args.steps},
                 "roofline": roofline,
