@@ -363,9 +363,17 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     // The pair kernel (cost in the same units): a key tile costs a pair 7 with one or two
     // query tiles (each CTA computes its 128 rows of an M = 256 MMA), a job switch 30, a
     // merge 100.
-    const int64_t kSwitch = pair ? 30 : 36, kMerge = pair ? 100 : 75;
+    // A schedule that cuts units runs past its bound by more than one that keeps them whole (the
+    // mergers wait for their pieces and read them at the end of the launch): 48 more at long,
+    // 82 more at short, measured on the single-CTA kernel.  Units are kept whole when the
+    // smallest bound without cuts is within kSplit of the smallest with them: short then runs
+    // 2 whole units per CTA (54.4 us against 59.5 with cuts), while long (bounds 791 / 875),
+    // page1 and mixed keep their cuts.
+    const int64_t kSwitch = pair ? 30 : 36, kMerge = pair ? 100 : 75, kSplit = pair ? 0 : 60;
     auto tile_cost = [pair](const GrAttnUnit& u) -> int64_t { return pair ? 7 : (u.nqt == 2 ? 20 : 17); };
-    // returns the CTAs used (n_cta + 1: does not fit); with emit, writes jobs and ranges
+    // returns the CTAs used (n_cta + 1: does not fit); with emit, writes jobs and ranges; with
+    // cut == false a unit that does not fit the rest of a CTA's budget moves whole to the next
+    bool cut = true;
     auto walk = [&](int64_t T, bool emit) -> int {
         int cta = 0, njobs = 0, job_begin = 0;
         int64_t load = 0;
@@ -389,7 +397,7 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
                 const int rem = u.n_tiles - t0;
                 int take = rem;
                 if (load + sw + merge + rem * tc > T) {
-                    const int64_t fit = (T - load - sw - merge) / tc;
+                    const int64_t fit = cut ? (T - load - sw - merge) / tc : 0;
                     if (fit < 1) {
                         if (njobs == 0) return n_cta + 1;  // not even one tile in an empty CTA
                         next_cta();
@@ -414,14 +422,21 @@ Schedule build_schedule(const gr_config* c, const gr_request* reqs, int n, int n
     };
     int64_t all = 0;
     for (auto& u : s.units) all += kMerge + kSwitch + u.n_tiles * tile_cost(u);
-    int64_t lo = 1, hi = all;  // hi: one CTA takes everything, which always fits
-    while (lo < hi) {
-        const int64_t mid = lo + (hi - lo) / 2;
-        if (walk(mid, false) <= n_cta) hi = mid;
-        else lo = mid + 1;
-    }
+    auto smallest_bound = [&]() {
+        int64_t lo = 1, hi = all;  // hi: one CTA takes everything, which always fits
+        while (lo < hi) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (walk(mid, false) <= n_cta) hi = mid;
+            else lo = mid + 1;
+        }
+        return lo;
+    };
+    const int64_t t_cut = smallest_bound();
+    cut = false;
+    const int64_t t_whole = kSplit > 0 ? smallest_bound() : t_cut + 1;
+    cut = !(t_whole <= t_cut + kSplit);
     s.cta_jobs.assign(n_cta, make_int2(0, 0));
-    walk(lo, true);
+    walk(cut ? t_cut : t_whole, true);
     (void)total;
     return s;
 }

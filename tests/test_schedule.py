@@ -110,6 +110,18 @@ def test_schedule_of_the_long_workload():
     assert len(ctas) == 76
 
 
+def test_short_units_are_kept_whole_when_cuts_gain_little():
+    """16 requests x ctx 1000 x beam 256: 256 units of 8 key tiles.  Whole units (two per CTA)
+    give a bound within the cut penalty of the cut schedule, so no unit is cut and every unit
+    is one job; the long workload (previous test) keeps its cuts."""
+    units, jobs, ctas = check_schedule(2, 8, [1000] * 16, [256] * 16, 152)
+    assert len(units) == 256 and np.all(units[:, 6] == 8)
+    assert np.all(units[:, 5] == 1) and len(jobs) == 256
+    assert np.max(ctas[:, 1] - ctas[:, 0]) == 2
+    # the pair kernel's schedule still cuts where that balances its pairs
+    check_schedule(2, 8, [1000] * 16, [256] * 16, 152, attn_kernel=2)
+
+
 def test_kernel_choice_and_pair_kernel_limits():
     """The automatic choice is the single-CTA kernel; the pair kernel needs head_dim 128."""
     _, _, c0 = B.attn_schedule(16, 8, [5000] * 8, [256] * 8, 152, head_dim=128, attn_kernel=0)
