@@ -39,6 +39,7 @@
 
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
+#include <float.h>
 #include <math_constants.h>
 #include <stdint.h>
 
@@ -80,7 +81,12 @@ __device__ __forceinline__ float cluster_row_lse(const float* __restrict__ x, in
     const int b0 = (int)((int64_t)n4 * part / kLogitCluster);
     const int b1 = (int)((int64_t)n4 * (part + 1) / kLogitCluster);
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    float m = -CUDART_INF_F, s = 0.f;
+    // Each term is exp2((x - m) * log2 e): the difference first, so that a value equal or close
+    // to the running max m gives an exact small argument whatever its magnitude (a product
+    // m * log2 e rounded on its own is off by ~1e22 at |m| ~ 1e30).  m starts at the most
+    // negative finite value, so that -inf logits add exactly 0 and a row of -inf has
+    // log-sum-exp -inf.
+    float m = -FLT_MAX, s = 0.f;
     int i = b0 + threadIdx.x;
     // 4 independent 16-byte loads in flight per thread
     for (; i + 3 * kLsThreads < b1; i += 4 * kLsThreads) {
@@ -91,18 +97,16 @@ __device__ __forceinline__ float cluster_row_lse(const float* __restrict__ x, in
         for (int u = 0; u < 4; ++u) {
             float cm = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
             if (cm > m) { s *= exp2f((m - cm) * CUDART_L2E_F); m = cm; }
-            const float ml = m * CUDART_L2E_F;
-            s += exp2f(fmaf(v[u].x, CUDART_L2E_F, -ml)) + exp2f(fmaf(v[u].y, CUDART_L2E_F, -ml)) +
-                 exp2f(fmaf(v[u].z, CUDART_L2E_F, -ml)) + exp2f(fmaf(v[u].w, CUDART_L2E_F, -ml));
+            s += exp2f((v[u].x - m) * CUDART_L2E_F) + exp2f((v[u].y - m) * CUDART_L2E_F) +
+                 exp2f((v[u].z - m) * CUDART_L2E_F) + exp2f((v[u].w - m) * CUDART_L2E_F);
         }
     }
     for (; i < b1; i += kLsThreads) {
         float4 v = __ldcs(x4 + i);
         float cm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
         if (cm > m) { s *= exp2f((m - cm) * CUDART_L2E_F); m = cm; }
-        const float ml = m * CUDART_L2E_F;
-        s += exp2f(fmaf(v.x, CUDART_L2E_F, -ml)) + exp2f(fmaf(v.y, CUDART_L2E_F, -ml)) +
-             exp2f(fmaf(v.z, CUDART_L2E_F, -ml)) + exp2f(fmaf(v.w, CUDART_L2E_F, -ml));
+        s += exp2f((v.x - m) * CUDART_L2E_F) + exp2f((v.y - m) * CUDART_L2E_F) +
+             exp2f((v.z - m) * CUDART_L2E_F) + exp2f((v.w - m) * CUDART_L2E_F);
     }
     if (part == kLogitCluster - 1) {  // ragged tail of a row whose length is not a multiple of 4
         for (int j = (n4 << 2) + threadIdx.x; j < V; j += kLsThreads) lse_merge(m, s, x[j], 1.f);

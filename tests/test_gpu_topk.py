@@ -129,3 +129,26 @@ def test_row_without_candidates_turns_the_threshold_bound_off():
     assert ls.beam.status(clear=True) == B.GR_ERR_DEVICE  # the NaN keys are reported
     res = ls.compare_topk(oinfo, lse_mode=True)
     assert not res["mismatch"] and res["n_sel"] == [W], res
+
+
+def test_minus_inf_and_huge_logits_outside_the_codes():
+    """Logit rows holding -inf (banned tokens) in whole blocks, including the first values of
+    each half a CTA reduces, and values of magnitude 1e30: the GPU's own log-sum-exp (no
+    lse_in) stays within 1e-4 of the oracle's float64 one and the selection is the oracle's.
+    The code logits stay ordinary, so every valid code keeps a finite log-probability."""
+    def edit(ls, t, x):
+        s = ls.spec
+        x = x.copy()
+        V = s.vocab
+        x[:, :2048] = -np.inf
+        x[:, V // 2:V // 2 + 1024] = -np.inf
+        x[:, 4096:4160] = -1e30
+        x[1::2, 2048:2052] = -np.inf
+        return x
+    spec = Spec(n_q_heads=2, n_kv_heads=1, head_dim=64, vocab=16384, n_levels=2, codes_per_level=256,
+                code_base=16384 - 512, ctx_lens=[8, 8], widths=[64, 32], n_items=[20000, 20000], seed=28)
+    ls = LockStep(spec, logits_fn=edit)
+    for t in range(2):
+        r = ls.topk_step(lse_mode=False)
+        assert r["lse_err"] <= LP_TOL and r["lp_err"] <= LP_TOL, (t, r)
+        assert not r["mismatch"], (t, r)

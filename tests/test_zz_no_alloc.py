@@ -117,6 +117,48 @@ def _assert_same(got, exp):
     assert np.max(np.abs(gk - ek), initial=0.0) <= LP_TOL
 
 
+def _level_rows(levels, seed=5):
+    """Keys that make the merge bucket its threshold bucket again (the first level's bucket
+    holds more than the 1024 keys it ranks directly, all distinct).  Every row's dominant
+    logit sits outside the codes and the code logits are at most -100, so each row's
+    log-sum-exp is 0 on the GPU and ~1e-43 in the oracle, and with zero beam scores every key
+    is its code logit on both sides.  64 rows x 128 codes, k = 100: 40 keys far above, for three
+    levels 30 more just above the band, 3000 consecutive float32 values (the band), the rest
+    below (-199..-198.5 for two levels, -1e30 for three: a wider first level), and two rows
+    of low keys only, so that the smallest row maximum leaves the band in range."""
+    n_rows, n_codes, vocab, code_lo = 64, 128, 1024, 512
+    rng = np.random.default_rng(seed)
+    x = np.full((n_rows, vocab), -1000.0, dtype=np.float32)
+    x[:, 0] = 0.0
+    high = (-100.0 - 0.25 * np.arange(40)).astype(np.float32)
+    mid = (-140.0 - 0.0625 * np.arange(30)).astype(np.float32) if levels == 3 else np.zeros(0, np.float32)
+    band = np.empty(3000, dtype=np.float32)
+    band[0] = -150.0
+    for i in range(1, len(band)):
+        band[i] = np.nextafter(band[i - 1], np.float32(0.0))
+    special = np.concatenate([high, mid, band])
+    n_main = (n_rows - 2) * n_codes
+    low = np.float32(-199.0 if levels == 2 else -1e30)
+    vals = np.full(n_main, low, dtype=np.float32)
+    if levels == 2:
+        vals = (low + 0.5 * rng.random(n_main)).astype(np.float32)
+    vals[:len(special)] = special
+    x[:n_rows - 2, code_lo:code_lo + n_codes] = vals[rng.permutation(n_main)].reshape(n_rows - 2, n_codes)
+    x[n_rows - 2:, code_lo:code_lo + n_codes] = low
+    return x, code_lo, n_codes
+
+
+@pytest.mark.parametrize("levels", [2, 3])
+def test_noalloc_threshold_bucketed_again(levels):
+    x, code_lo, C = _level_rows(levels)
+    mask = _full_mask(x.shape[0], C)
+    exp = _oracle(x, None, mask, code_lo, C, 100)
+    assert len(exp[0]) == 100
+    got = _run(x, None, mask, code_lo, C, 100)
+    _assert_same(got, exp)
+    assert np.array_equal(got[2].view(np.uint32), exp[2].view(np.uint32))  # keys bit for bit
+
+
 def test_noalloc_matches_constrained_topk_twice():
     import torch
     C = 256
