@@ -117,16 +117,16 @@ def _assert_same(got, exp):
     assert np.max(np.abs(gk - ek), initial=0.0) <= LP_TOL
 
 
-def _level_rows(levels, seed=5):
+def _level_rows(levels, seed=5, n_rows=64, n_codes=128):
     """Keys that make the merge bucket its threshold bucket again (the first level's bucket
     holds more than the 1024 keys it ranks directly, all distinct).  Every row's dominant
     logit sits outside the codes and the code logits are at most -100, so each row's
     log-sum-exp is 0 on the GPU and ~1e-43 in the oracle, and with zero beam scores every key
-    is its code logit on both sides.  64 rows x 128 codes, k = 100: 40 keys far above, for three
+    is its code logit on both sides.  64 rows x 128 codes by default, k = 100: 40 keys far above, for three
     levels 30 more just above the band, 3000 consecutive float32 values (the band), the rest
     below (-199..-198.5 for two levels, -1e30 for three: a wider first level), and two rows
     of low keys only, so that the smallest row maximum leaves the band in range."""
-    n_rows, n_codes, vocab, code_lo = 64, 128, 1024, 512
+    vocab, code_lo = 2 * max(512, n_codes), max(512, n_codes)
     rng = np.random.default_rng(seed)
     x = np.full((n_rows, vocab), -1000.0, dtype=np.float32)
     x[:, 0] = 0.0
@@ -148,15 +148,30 @@ def _level_rows(levels, seed=5):
     return x, code_lo, n_codes
 
 
-@pytest.mark.parametrize("levels", [2, 3])
-def test_noalloc_threshold_bucketed_again(levels):
-    x, code_lo, C = _level_rows(levels)
+@pytest.mark.parametrize("levels,n_rows,n_codes", [(2, 64, 128), (3, 64, 128), (3, 256, 1024)])
+def test_noalloc_threshold_bucketed_again(levels, n_rows, n_codes):
+    # 256 x 1024 candidates: 32768 per CTA, more than its shared-memory stage, so every pass
+    # re-reads the keys from global memory
+    x, code_lo, C = _level_rows(levels, n_rows=n_rows, n_codes=n_codes)
     mask = _full_mask(x.shape[0], C)
     exp = _oracle(x, None, mask, code_lo, C, 100)
     assert len(exp[0]) == 100
     got = _run(x, None, mask, code_lo, C, 100)
     _assert_same(got, exp)
     assert np.array_equal(got[2].view(np.uint32), exp[2].view(np.uint32))  # keys bit for bit
+
+
+def test_noalloc_all_keys_equal_in_shared_memory():
+    """8192 candidates with one key value (constant logits): the first level's bucket is a
+    single value holding more keys than are ranked directly, so the first k in flat order are
+    taken, from the keys staged in shared memory."""
+    n_rows, C, vocab, code_lo = 64, 128, 1024, 512
+    x = np.zeros((n_rows, vocab), dtype=np.float32)
+    mask = _full_mask(n_rows, C)
+    exp = _oracle(x, None, mask, code_lo, C, 100)
+    got = _run(x, None, mask, code_lo, C, 100)
+    _assert_same(got, exp)
+    assert np.array_equal(got[0], np.zeros(100, np.int32)) and np.array_equal(got[1], np.arange(100))
 
 
 def test_noalloc_matches_constrained_topk_twice():
