@@ -658,6 +658,7 @@ gr_status build_tables(gr_beam* h) {
     h->st.n_units = (int)h->sched.units.size();
     h->st.n_jobs = (int)h->sched.jobs.size();
     h->st.n_cta = (int)h->sched.cta_jobs.size();
+    h->st.n_sm = h->n_sm;
     return GR_OK;
 }
 }  // namespace

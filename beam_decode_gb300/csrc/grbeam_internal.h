@@ -108,6 +108,7 @@ struct GrState {
     int n_units, n_jobs, n_cta;  // n_cta: CTAs, or CTA pairs when attn_pair
     int attn_pair;      // the decode attention runs on CTA pairs (k_pair_attn)
     int attn_one;       // every unit has one query tile: the single-CTA kernel double-buffers S
+    int n_sm;           // SMs of the device (the top-K merge sizes its clusters by it)
     float* o_part;      // [n_jobs][D][kUnitRows] pieces of split units (later key ranges), column-major
     float* lse_part;    // [n_jobs][kUnitRows]
     uint32_t* piece_flag; // [n_jobs][kUnitRows] 1 = piece row published and not yet merged

@@ -18,7 +18,8 @@
 //     keys (rank counted against the row's other keys, same order) and
 //     clears the rest.  The global top W is unchanged: every key above a
 //     selected key in its own row is selected too.
-//   stage 2 (cross-beam merge, one cluster of kMergeCTAs CTAs per request):
+//   stage 2 (cross-beam merge, one cluster of 8 CTAs per request, or of 4 when
+//     the requests' clusters of 8 would not fit the GPU at once):
 //     each CTA takes a contiguous flat range of the request's keys into shared
 //     memory.  The threshold -- the W-th largest key -- is found by
 //     range-adaptive bucketing: kNB equal-width buckets over [a0, largest
@@ -234,7 +235,7 @@ __device__ __forceinline__ bool gather_row(const float* __restrict__ xc, const u
 // ---------------------------------------------------------------------------
 // stage 2: cross-beam merge
 // ---------------------------------------------------------------------------
-constexpr int kMergeCTAs = 8;         // one portable cluster per request
+constexpr int kMergeCTAs = 8;         // the largest cluster of a request (portable)
 constexpr int kNBBits = 8;
 constexpr int kNB = 1 << kNBBits;     // buckets per level (one per thread)
 constexpr int kMergeThreads = kNB;
@@ -321,12 +322,13 @@ __device__ __forceinline__ unsigned long long peer_ld64(uint32_t a) {
 }
 
 // The top-min(k_want, #candidates) of N ordered keys (flat order, 0 = no candidate) of one
-// request, in (key desc, flat asc) order.  Called by every CTA of a kMergeCTAs cluster with
-// the same arguments; `stage` is kMergeStage uint32 of shared memory.  range[0..1] =
+// request, in (key desc, flat asc) order.  Called by every CTA of a cluster of kC CTAs
+// (kC <= kMergeCTAs) with the same arguments; `stage` is kMergeStage uint32 of shared memory.  range[0..1] =
 // (~lower, upper) bound of the candidate keys and range[2] = ~(the smallest of the N / C rows'
 // largest keys), all raised by stage 1 (gather_row); any bounds that contain every candidate
 // and lie at or below that smallest maximum give the same result.  The merge sets the three
 // words back to 0 for the next call once every CTA has read them.
+template <int kC = kMergeCTAs>
 __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, int N, int C, int k_want,
                                              uint32_t* __restrict__ range, const MergeOut out, uint32_t* stage,
                                              MergeSmem& sm) {
@@ -334,8 +336,8 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
     cg::cluster_group cl = cg::this_cluster();
     const int cr = (int)cl.block_rank();
     const int tid = threadIdx.x;
-    const int lo = (int)((int64_t)N * cr / kMergeCTAs);
-    const int n = (int)((int64_t)N * (cr + 1) / kMergeCTAs) - lo;
+    const int lo = (int)((int64_t)N * cr / kC);
+    const int n = (int)((int64_t)N * (cr + 1) / kC) - lo;
     const uint32_t* g = keys + lo;
     const bool staged = n <= kMergeStage;
     // Every pass visits the CTA's keys; a range too long for shared memory is re-read from
@@ -445,7 +447,7 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
             // is descending bucket order)
             int tsum = 0;
 #pragma unroll
-            for (int r = 0; r < kMergeCTAs; ++r) tsum += peer_ld(peer_addr(&h[jb], r));
+            for (int r = 0; r < kC; ++r) tsum += peer_ld(peer_addr(&h[jb], r));
             int total;
             const int incl = block_incl_scan(tsum, sm.warp_tot, total);
             if (level == 0) {
@@ -549,14 +551,14 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
     }
     cl.sync();
     // gather every CTA's lists (offsets in cluster rank order)
-    if (tid < kMergeCTAs) {
+    if (tid < kC) {
         sm.len_s[tid] = peer_ld(peer_addr(&sm.n_sure, tid));
         sm.len_t[tid] = peer_ld(peer_addr(&sm.n_thr, tid));
     }
     __syncthreads();
     if (tid == 0) {
         int os = 0, ot = 0;
-        for (int r = 0; r < kMergeCTAs; ++r) {
+        for (int r = 0; r < kC; ++r) {
             sm.off_s[r] = os;
             sm.off_t[r] = ot;
             os += sm.len_s[r];
@@ -570,14 +572,14 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
     // every entry of every CTA's two lists at once: entry j of the concatenation (sure lists in
     // rank order, then bucket lists) comes from the CTA whose block holds it
     {
-        const int tot_s = sm.off_s[kMergeCTAs - 1] + sm.len_s[kMergeCTAs - 1];
+        const int tot_s = sm.off_s[kC - 1] + sm.len_s[kC - 1];
         const int tot = tot_s + (ranked ? n_thr : 0);
         for (int j = tid; j < tot; j += kMergeThreads) {
             const bool is_s = j < tot_s;
             const int jj = is_s ? j : j - tot_s;
             int r = 0;
 #pragma unroll
-            for (int k = 1; k < kMergeCTAs; ++k) r += jj >= (is_s ? sm.off_s[k] : sm.off_t[k]);
+            for (int k = 1; k < kC; ++k) r += jj >= (is_s ? sm.off_s[k] : sm.off_t[k]);
             const int i = jj - (is_s ? sm.off_s[r] : sm.off_t[r]);
             const uint32_t pa = peer_addr(is_s ? (const void*)(sm.sure + i) : (const void*)(sm.thr + i), r);
             (is_s ? s_sure : s_thr)[jj] = peer_ld64(pa);
@@ -616,8 +618,8 @@ __device__ __forceinline__ void merge_select(const uint32_t* __restrict__ keys, 
     // entry's is n_sure + the number of bucket entries above it, and it is taken when below kk
     constexpr int kSplit = 8;  // threads counting for one entry
     auto rank_list = [&](const unsigned long long* list, int len, int pos0, int limit) {
-        const int r0 = (int)((int64_t)len * cr / kMergeCTAs);
-        const int r1 = (int)((int64_t)len * (cr + 1) / kMergeCTAs);
+        const int r0 = (int)((int64_t)len * cr / kC);
+        const int r1 = (int)((int64_t)len * (cr + 1) / kC);
         for (int base = r0 * kSplit; base < r1 * kSplit; base += kMergeThreads) {
             const int idx = base + tid;
             const int e = idx / kSplit, part = idx % kSplit;

@@ -152,3 +152,15 @@ def test_minus_inf_and_huge_logits_outside_the_codes():
         r = ls.topk_step(lse_mode=False)
         assert r["lse_err"] <= LP_TOL and r["lp_err"] <= LP_TOL, (t, r)
         assert not r["mismatch"], (t, r)
+
+
+def test_many_requests_merge_in_smaller_clusters():
+    """40 requests: their clusters of 8 merge CTAs would not fit the GPU at once (two per SM),
+    so each request is merged by a cluster of 4; selections against the oracle, exact ties
+    included (quantised logits), over two levels."""
+    spec = Spec(vocab=2048, n_levels=3, codes_per_level=64, code_base=2048 - 192, ctx_lens=[8] * 40,
+                widths=[48] * 40, n_items=[3000] * 40, seed=29)
+    ls = LockStep(spec, logits_fn=lambda ls, t, x: np.round(x * 4.0) / 4.0)
+    for t in range(3):
+        r = ls.topk_step(lse_mode=True)
+        assert not r["mismatch"], (t, r)
